@@ -1,0 +1,342 @@
+"""Benchmark of the quantized sparse MoE layer forward on one GB300 (or N independent replicas).
+
+Default workload: the GLM-5.2-class decode layer (d=7168, d_ff=2048, 256 experts,
+top-8, int4 group-128 weights, routed scale 2.5, bias 0, bf16 x), T=1 token per
+step, with the T=4 variant reported alongside.  A step is one full layer
+forward (router, grouping, gate/up + SwiGLU, down, combine) on a fresh x, so
+routing differs every step; the 5.9 GB expert set is far larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|mtp_verify|prefill|stacked]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores (CPU baseline arm)
+
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import harness as H  # noqa: E402
+
+METRIC = "MoE-layer tokens/s and HBM GB/s (decode) / tensor % peak (prefill) on 1 GB300"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks sampling
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+
+def workload_setup(name: str):
+    w = H.WORKLOADS[name]
+    if name == "decode":
+        return w, 1, (1, 4)
+    if name == "mtp_verify":
+        return w, 3, (3,)
+    if name == "prefill":
+        return w, 2048, (2048,)
+    if name == "stacked":
+        return w, 256, (256,)
+    raise ValueError(name)
+
+
+def unique_expert_bytes(dl, T) -> tuple[int, int]:
+    """(gate+up bytes, down bytes) streamed by the last forward: unique routed experts + shared."""
+    idx = dl.routing(T)[0]
+    U = len(np.unique(idx))
+    L = dl.layer
+    gu = L.experts.gate.nbytes // L.E + L.experts.up.nbytes // L.E
+    dn = L.experts.down.nbytes // L.E
+    gub, dnb = U * gu, U * dn
+    if L.shared is not None:
+        gub += L.shared.gate.nbytes + L.shared.up.nbytes
+        dnb += L.shared.down.nbytes
+    return gub, dnb
+
+
+def bench_native(args, rank: int, world: int):
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+
+    coli.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w, T_main, Ts = workload_setup(args.workload)
+    if args.workload == "stacked":
+        raise SystemExit("stacked bench: use tests (per-layer parity); bench reports single layers")
+    t0 = time.time()
+    layer = w.layer(0)
+    dl = DeviceLayer(layer, max(Ts), device=dev)
+    gen_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+    pk = peaks()
+    results = {}
+    for T in Ts:
+        nx = K + W
+        xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(nx)]
+        out = torch.empty((T, layer.d), dtype=torch.float32, device=dev)
+        for i in range(W):
+            dl.forward(xs[i], out=out)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        # ---- timed region (device time, CUDA events on the launching stream)
+        with ClockSampler(dev.index) as clk:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for i in range(K):
+                dl.forward(xs[W + i], out=out)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1)
+        launches = dl.plan.last_launch_count()
+        # ---- per-kernel times (same steps again, kernel-boundary events recorded by the library)
+        dl.plan.profile_begin(K)
+        for i in range(K):
+            dl.forward(xs[W + i], out=out)
+        torch.cuda.synchronize(dev)
+        kt = dl.plan.profile_end()
+        # algorithmic bytes of the gate/up and down kernels for these K steps
+        gub, dnb = 0, 0
+        for i in range(K):
+            dl.forward(xs[W + i], out=out)
+            torch.cuda.synchronize(dev)
+            a, b = unique_expert_bytes(dl, T)
+            gub += a
+            dnb += b
+        # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
+        xh = [torch.empty_like(xs[0], device="cpu").pin_memory() for _ in range(K)]
+        for i in range(K):
+            xh[i].copy_(xs[W + i].cpu())
+        oh = torch.empty((K, T, layer.d), dtype=torch.float32).pin_memory()
+        xd = torch.empty_like(xs[0])
+        torch.cuda.synchronize(dev)
+        t_e2e0 = time.perf_counter()
+        for i in range(K):
+            xd.copy_(xh[i], non_blocking=True)
+            dl.forward(xd, out=out)
+            oh[i].copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_s = time.perf_counter() - t_e2e0
+        results[T] = dict(ms=ms, kt=kt, launches=launches, gub=gub, dnb=dnb, clocks=clk.summary(), e2e_s=e2e_s,
+                          h2d=xh[0].numel() * xh[0].element_size(), d2h=T * layer.d * 4)
+        del xs
+    # reduce over ranks: max time
+    def mx(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    lines = {}
+    for T, r in results.items():
+        ms_tot = mx(r["ms"])
+        e2e_tot = mx(r["e2e_s"])
+        kt = r["kt"]
+        gu_ms, gu_n = kt.get("expert_gate_up", (0.0, 0))
+        dn_ms, dn_n = kt.get("expert_down", (0.0, 0))
+        step_kernel_ms = sum(v[0] for v in kt.values()) / K
+        achieved = (r["gub"] / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
+        achieved_d = (r["dnb"] / dn_n) / (dn_ms / dn_n * 1e-3) / 1e9 if dn_n else None
+        layer_gbs = (r["gub"] + r["dnb"]) / K / (ms_tot / K * 1e-3) / 1e9
+        lines[T] = {
+            "metric": METRIC,
+            "value": world * K * T / (ms_tot * 1e-3),
+            "unit": "tokens/s",
+            "ms_per_step": ms_tot / K,
+            "hbm_gbs_layer": layer_gbs,
+            "hbm_frac_layer": layer_gbs / pk["hbm_gbs"],
+            "roofline": {"bound": "hbm", "kernel": "expert_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                         "traffic": None, "peak_source": pk["source"],
+                         "algorithmic_bytes_per_launch": r["gub"] / max(gu_n, 1),
+                         "down_kernel_achieved_gbs": achieved_d},
+            "kernel_ms_per_step": {k: v[0] / v[1] for k, v in kt.items()},
+            "kernel_share": {k: v[0] / max(sum(x[0] for x in kt.values()), 1e-12) for k, v in kt.items()},
+            "kernel_sum_ms_per_step": step_kernel_ms,
+            "e2e": {"value": world * K * T / e2e_tot, "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]},
+            "gpu_launches": K * r["launches"],
+            "clocks": r["clocks"],
+        }
+    return w, T_main, Ts, lines, gen_s
+
+
+def cpu_baseline(w, T: int, budget_s: float = 12.0):
+    """The oracle as it stands on this host's cores, on a bounded sample of the workload's tokens."""
+    import oracle as O
+    layer = w.layer(0)
+    orc = O.Oracle(layer)
+    cores = O.default_threads()
+    n_tok = max(1, cores)
+    x = w.x(max(T, n_tok), 77)
+    t0 = time.perf_counter()
+    done = 0
+    while True:
+        orc.forward(x, tokens=np.arange(done % x.shape[0], done % x.shape[0] + 1, dtype=np.int32) if n_tok == 1
+                    else np.arange(n_tok, dtype=np.int32) % x.shape[0], nthreads=cores)
+        done += n_tok
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} tokens of the {w.name} workload (d={w.d}, d_ff={w.F}, E={w.E}, k={w.k}), "
+                      f"{n_tok} tokens per call over {cores} threads, {dt:.1f} s"}, layer
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "mtp_verify", "prefill", "stacked"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    w, T_main, Ts = None, None, None
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        w, T_main, Ts = workload_setup(args.workload)
+        import oracle as O
+        layer = w.layer(0)
+        orc = O.Oracle(layer)
+        cores = O.default_threads()
+        n_tok = max(1, min(cores, 16))
+        x = w.x(max(n_tok, T_main), 77)
+        toks = np.arange(n_tok, dtype=np.int32) % x.shape[0]
+        for _ in range(args.warmup):
+            orc.forward(x, tokens=toks[:1], nthreads=cores)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            orc.forward(x, tokens=toks, nthreads=cores)
+        dt = time.perf_counter() - t0
+        v = args.steps * n_tok / dt
+        sample = f"{n_tok} tokens per step of the {w.name} workload, {cores} threads"
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic",
+                          "config": {"workload": f"{w.name} (T={T_main})", "d": w.d, "d_ff": w.F, "E": w.E,
+                                     "k": w.k},
+                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                           "sample": sample},
+                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    w, T_main, Ts, lines, gen_s = bench_native(args, rank, world)
+    if rank != 0:
+        return
+    line = dict(lines[T_main])
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu, _ = cpu_baseline(w, T_main)
+    line.update({
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int4-weights/f32-accumulate" if w.qtypes[0] == 0 else "int8",
+        "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
+        "config": {"workload": f"{w.name}: GLM-5.2-class MoE layer, T={T_main} tokens per step",
+                   "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho,
+                   "qtype": "int4-g128" if w.qtypes[0] == 0 else "int8-pc",
+                   "shared_expert_d_ff": w.F_shared, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 5.9 GB expert set, fresh x (fresh routing) every step",
+                   "host_generation_s": round(gen_s, 1)},
+        "cpu_baseline": cpu,
+    })
+    line["variants"] = {f"T={T}": {k: lines[T][k] for k in ("value", "ms_per_step", "hbm_gbs_layer",
+                                                            "hbm_frac_layer", "roofline", "kernel_ms_per_step",
+                                                            "e2e", "gpu_launches")}
+                        for T in Ts if T != T_main}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

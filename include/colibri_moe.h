@@ -1,0 +1,221 @@
+/*
+ * colibri_moe.h -- C ABI of a quantized sparse Mixture-of-Experts layer
+ * forward for one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The layer (the MoE hot path of the Colibri engine):
+ *   1. router: logits z = x Wr^T, s = sigmoid(z), u = s + bias; the k experts
+ *      with the largest u are chosen ("25GB RAM runs 744B GLM-5.2" page
+ *      (pwwt.cn), section 3.1: DeepSeek-V3 style sigmoid router, 8 of 256
+ *      experts per token; section 4.3: the expert bias of auxiliary-loss-free
+ *      balancing steers selection).  Ties go to the lower expert id.
+ *   2. gate weights g = routed_scale * s / sum(s over the chosen experts).
+ *   3. batch-union grouping (same page, section 3.4): (token, slot) pairs are
+ *      grouped by expert, so each chosen expert's weights are streamed once
+ *      for all of its tokens.
+ *   4. per-expert SwiGLU FFN y = Wd (silu(Wg x) * (Wu x)) on int4 / int8
+ *      weights with per-output-channel scale and zero-point ("Colibri
+ *      walkthrough" page (discosf.com), section 3.4): w = (q - zp) * scale.
+ *   5. optional always-on shared expert ("25GB RAM" page, section 2), weight 1.
+ *   6. out[t] = residual[t] + sum_j g[t][j] * y[t][j] + y_shared[t].
+ *
+ * Conventions for every call:
+ *   - Pointers named "device" are CUDA device (or managed) pointers of the
+ *     current device; "host" pointers are ordinary CPU memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls that take a stream are asynchronous on it and never
+ *     synchronise the host.
+ *   - Errors are returned as coli_status; nothing aborts or throws.  The
+ *     message of the last error on the calling thread is returned by
+ *     colibri_moe_last_error().  Argument checks happen before any launch.
+ *   - The caller owns every tensor and the workspace.  A plan owns only its
+ *     host metadata and a small device table of expert descriptors that it
+ *     frees in colibri_moe_destroy().
+ */
+#ifndef COLIBRI_MOE_H
+#define COLIBRI_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* exported symbols of the shared library */
+#if defined(__GNUC__)
+#define COLI_API __attribute__((visibility("default")))
+#else
+#define COLI_API
+#endif
+
+typedef enum {
+  COLI_OK = 0,
+  COLI_EINVAL = 1,          /* bad shape, null pointer, T out of range */
+  COLI_EALIGN = 2,          /* a pointer is not aligned as documented */
+  COLI_EUNSUPPORTED = 3,    /* valid request this build cannot serve (qtype, sizes) */
+  COLI_EWORKSPACE = 4,      /* workspace smaller than colibri_moe_plan reported */
+  COLI_ECUDA = 5,           /* a CUDA runtime call failed (message has the CUDA error) */
+  COLI_EDEVICE = 6,         /* a kernel reported an error in the workspace status word */
+  COLI_ESTATE = 7           /* call out of order (e.g. forward before bind) */
+} coli_status;
+
+typedef enum {
+  /* int4 codes, groups of 128 consecutive inputs of one output row share an
+     fp16 scale and a 4-bit zero-point */
+  COLI_Q_INT4_G128 = 0,
+  /* int8 codes, one fp32 scale and one 8-bit zero-point per output row */
+  COLI_Q_INT8_PC = 1
+} coli_qtype;
+
+typedef enum { COLI_X_BF16 = 0, COLI_X_F32 = 1 } coli_xtype;
+
+/*
+ * One quantised matrix W[N][K] (N output rows, K inputs), device pointers.
+ *   COLI_Q_INT4_G128: q     uint8 [N][K/2], byte j of a row holds inputs 2j
+ *                           (low nibble) and 2j+1 (high nibble);
+ *                     scale fp16 [N][K/128];
+ *                     zp    uint8 [N][ceil(K/256)], low nibble = even group.
+ *   COLI_Q_INT8_PC:   q     uint8 [N][K]; scale float [N]; zp uint8 [N].
+ * Dequantised weight: (code - zero_point) * scale.
+ * q must be 16-byte aligned (it is streamed with TMA); scale and zp need only
+ * their element alignment.
+ */
+typedef struct {
+  const void* q;
+  const void* scale;
+  const void* zp;
+} coli_qmat;
+
+/* One expert: gate and up are [d_ff][d], down is [d][d_ff]. */
+typedef struct {
+  coli_qmat gate, up, down;
+} coli_expert;
+
+/*
+ * Layer description.
+ *   T_max       largest token count a forward call may pass (>= 1).
+ *   d           hidden size; d_ff the routed experts' FFN size.
+ *   E, k        number of routed experts and experts chosen per token
+ *               (1 <= k <= min(E, 32), E <= 1024).
+ *   routed_scale the factor applied to the renormalised gate weights.
+ *   qtype       coli_qtype of every expert matrix (shared expert included).
+ *   xtype       coli_xtype of x.
+ *   has_shared  1 = one always-on shared expert with FFN size shared_d_ff.
+ * Sizes supported by the kernels: d and the FFN sizes are multiples of 256
+ * (int4) or 128 (int8).
+ */
+typedef struct {
+  int T_max;
+  int d;
+  int d_ff;
+  int E;
+  int k;
+  float routed_scale;
+  int qtype;
+  int xtype;
+  int has_shared;
+  int shared_d_ff;
+} coli_moe_desc;
+
+typedef struct coli_moe_plan coli_moe_plan_t;
+
+/*
+ * Validate `desc` and create a plan (host memory only; no CUDA call).
+ * *workspace_bytes receives the size of the device workspace a forward call
+ * needs for up to T_max tokens (256-byte aligned base required).
+ * Errors: COLI_EINVAL (null argument, bad sizes), COLI_EUNSUPPORTED.
+ */
+COLI_API coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, size_t* workspace_bytes);
+
+/*
+ * Bind the expert weights (the resident "expert slots") to a plan on the
+ * current device.  experts: HOST array [E] of descriptors holding device
+ * pointers; shared: HOST pointer to one descriptor, or NULL when the plan has
+ * no shared expert.  The weights themselves are not copied: they must stay
+ * allocated and unchanged while the plan is used.  Synchronous: builds the
+ * TMA tensor maps and uploads the descriptor table (plan-owned device memory,
+ * freed by colibri_moe_destroy).  May be called again to rebind.
+ * Errors: COLI_EINVAL (null pointer), COLI_EALIGN (q not 16-byte aligned),
+ * COLI_ECUDA.
+ */
+COLI_API coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* experts, const coli_expert* shared);
+
+/*
+ * One layer forward for T tokens (1 <= T <= T_max), asynchronous on stream.
+ *   x         device [T][d], bf16 or fp32 per desc.xtype (16-byte aligned).
+ *   router_w  device float [E][d] (16-byte aligned).
+ *   bias      device float [E]: selection-only router bias.
+ *   residual  device float [T][d] added to the output, or NULL.  May equal out.
+ *   out       device float [T][d].
+ *   workspace device, >= the size colibri_moe_plan reported, 256-byte aligned.
+ * Two calls that overlap on the GPU need two workspaces.
+ * Errors: COLI_EINVAL, COLI_EALIGN, COLI_EWORKSPACE, COLI_ESTATE (not bound),
+ * COLI_ECUDA (launch failure).
+ */
+COLI_API coli_status colibri_moe_forward(const coli_moe_plan_t* plan, int T, const void* x, const float* router_w,
+                                const float* bias, const float* residual, float* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
+ * RMSNorm with unit gain, rounded to bf16 (the input of the next stacked
+ * layer): out[t][i] = bf16(h[t][i] / sqrt(mean_i(h[t][i]^2) + eps)).
+ * h device float [T][d]; out device uint16 (bf16 bits) [T][d]; d % 4 == 0.
+ */
+COLI_API coli_status colibri_moe_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, void* stream);
+
+/*
+ * Copy the routing state of the last forward that used `workspace` into
+ * caller buffers (device pointers, any may be NULL), asynchronously on stream:
+ *   topk_idx int32 [T][k]  chosen experts, ascending ids per token
+ *   topk_w   float [T][k]  gate weights in the same order
+ *   near_tie int32 [T]     1 where the k-th and (k+1)-th selection scores
+ *                          differ by less than 1e-5
+ *   expert_offsets int32 [E+1]  start of each expert's pairs in grouped order
+ *   pair_token, pair_slot int32 [T*k]  (token, slot) of each grouped pair,
+ *                          sorted by (expert, token, slot)
+ * Errors: COLI_EINVAL, COLI_ECUDA.
+ */
+COLI_API coli_status colibri_moe_debug_routing(const coli_moe_plan_t* plan, const void* workspace, int T, int32_t* topk_idx,
+                                      float* topk_w, int32_t* near_tie, int32_t* expert_offsets, int32_t* pair_token,
+                                      int32_t* pair_slot, void* stream);
+
+/*
+ * Read the device status word of `workspace` (synchronises `stream`).
+ * *device_status = 0 when the last forward ran clean; otherwise a bit set of
+ * COLI_DEV_* flags.  Returns COLI_EDEVICE when the word is non-zero.
+ */
+#define COLI_DEV_BAD_EXPERT_ID 1   /* a router index outside [0, E) reached the grouping step */
+#define COLI_DEV_WAIT_TIMEOUT 2    /* a pipeline wait gave up after its time limit (~1 s) */
+COLI_API coli_status colibri_moe_check_status(const coli_moe_plan_t* plan, const void* workspace, int32_t* device_status,
+                                     void* stream);
+
+/*
+ * Per-kernel timing (the per-stage share that a "--profile" run reports).
+ * colibri_moe_profile_begin(plan, max_calls) makes the next forward calls
+ * record a CUDA event before and after every kernel, on the launching stream,
+ * for up to max_calls calls.  colibri_moe_profile_end() synchronises those
+ * events, writes up to max_kernels entries of {name, total ms, launches}
+ * (names are static strings owned by the library) and returns the number of
+ * distinct kernels in *n_kernels; profiling is then off.
+ */
+typedef struct {
+  const char* name;
+  double total_ms;
+  int launches;
+} coli_kernel_time;
+COLI_API coli_status colibri_moe_profile_begin(coli_moe_plan_t* plan, int max_calls);
+COLI_API coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out, int max_kernels, int* n_kernels);
+
+/* Number of kernel launches the last forward call of this plan issued. */
+COLI_API int colibri_moe_last_launch_count(const coli_moe_plan_t* plan);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+COLI_API const char* colibri_moe_last_error(void);
+
+/* Free a plan and its device descriptor table.  NULL is ignored. */
+COLI_API void colibri_moe_destroy(coli_moe_plan_t* plan);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLIBRI_MOE_H */

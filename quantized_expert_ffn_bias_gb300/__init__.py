@@ -1,0 +1,203 @@
+"""Python binding of the quantized sparse MoE layer library (libcolibri_moe.so).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  Functions keep the C names (``colibri_moe_*``); the ``Plan`` class
+wraps a plan handle.  Pointers are plain integers or objects with a
+``data_ptr()`` method (for example torch tensors); streams are integers
+(``torch.cuda.Stream.cuda_stream``) or objects with a ``cuda_stream`` attribute.
+
+There is no CPU fallback: if the library has not been built, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_EUNSUPPORTED, COLI_EWORKSPACE, COLI_ECUDA, COLI_EDEVICE, COLI_ESTATE = range(8)
+COLI_Q_INT4_G128, COLI_Q_INT8_PC = 0, 1
+COLI_X_BF16, COLI_X_F32 = 0, 1
+COLI_DEV_BAD_EXPERT_ID, COLI_DEV_WAIT_TIMEOUT = 1, 2
+
+LIB_PATH = _build.LIB
+_lock = threading.Lock()
+_lib = None
+
+
+class ColiError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"colibri_moe error {status}: {msg}")
+        self.status = status
+
+
+class coli_qmat(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("zp", ctypes.c_void_p)]
+
+
+class coli_expert(ctypes.Structure):
+    _fields_ = [("gate", coli_qmat), ("up", coli_qmat), ("down", coli_qmat)]
+
+
+class coli_moe_desc(ctypes.Structure):
+    _fields_ = [("T_max", ctypes.c_int), ("d", ctypes.c_int), ("d_ff", ctypes.c_int), ("E", ctypes.c_int),
+                ("k", ctypes.c_int), ("routed_scale", ctypes.c_float), ("qtype", ctypes.c_int),
+                ("xtype", ctypes.c_int), ("has_shared", ctypes.c_int), ("shared_d_ff", ctypes.c_int)]
+
+
+class coli_kernel_time(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("total_ms", ctypes.c_double), ("launches", ctypes.c_int)]
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library for sm_103a (in-tree)."""
+    return _build.build(force=force)
+
+
+def lib():
+    """Load libcolibri_moe.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built ({LIB_PATH}); run quantized_expert_ffn_bias_gb300.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+            st = ctypes.c_int
+            L.colibri_moe_plan.argtypes = [ctypes.POINTER(coli_moe_desc), ctypes.POINTER(vp), ctypes.POINTER(sz)]
+            L.colibri_moe_plan.restype = st
+            L.colibri_moe_bind_experts.argtypes = [vp, ctypes.POINTER(coli_expert), ctypes.POINTER(coli_expert)]
+            L.colibri_moe_bind_experts.restype = st
+            L.colibri_moe_forward.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.colibri_moe_forward.restype = st
+            L.colibri_moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
+            L.colibri_moe_rmsnorm_bf16.restype = st
+            L.colibri_moe_debug_routing.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
+            L.colibri_moe_debug_routing.restype = st
+            L.colibri_moe_check_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32), vp]
+            L.colibri_moe_check_status.restype = st
+            L.colibri_moe_profile_begin.argtypes = [vp, i32]
+            L.colibri_moe_profile_begin.restype = st
+            L.colibri_moe_profile_end.argtypes = [vp, ctypes.POINTER(coli_kernel_time), i32, ctypes.POINTER(i32)]
+            L.colibri_moe_profile_end.restype = st
+            L.colibri_moe_last_launch_count.argtypes = [vp]
+            L.colibri_moe_last_launch_count.restype = i32
+            L.colibri_moe_last_error.argtypes = []
+            L.colibri_moe_last_error.restype = ctypes.c_char_p
+            L.colibri_moe_destroy.argtypes = [vp]
+            L.colibri_moe_destroy.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(v) -> int | None:
+    if v is None:
+        return None
+    if isinstance(v, int):
+        return v
+    return int(v.data_ptr())
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(rc: int):
+    if rc != COLI_OK:
+        raise ColiError(rc, lib().colibri_moe_last_error().decode(errors="replace"))
+
+
+def colibri_moe_last_error() -> str:
+    return lib().colibri_moe_last_error().decode(errors="replace")
+
+
+def colibri_moe_rmsnorm_bf16(h, T: int, d: int, eps: float, out, stream=None):
+    _check(lib().colibri_moe_rmsnorm_bf16(_ptr(h), T, d, eps, _ptr(out), _stream(stream)))
+
+
+def qmat(q, scale, zp) -> coli_qmat:
+    return coli_qmat(_ptr(q), _ptr(scale), _ptr(zp))
+
+
+class Plan:
+    """A validated layer plan (colibri_moe_plan) with its bound experts."""
+
+    def __init__(self, *, T_max: int, d: int, d_ff: int, E: int, k: int, routed_scale: float, qtype: int,
+                 xtype: int, has_shared: bool = False, shared_d_ff: int = 0):
+        self.desc = coli_moe_desc(T_max, d, d_ff, E, k, routed_scale, qtype, xtype, 1 if has_shared else 0,
+                                  shared_d_ff)
+        h = ctypes.c_void_p()
+        nbytes = ctypes.c_size_t()
+        _check(lib().colibri_moe_plan(ctypes.byref(self.desc), ctypes.byref(h), ctypes.byref(nbytes)))
+        self.handle = h.value
+        self.workspace_bytes = nbytes.value
+
+    def colibri_moe_bind_experts(self, experts, shared=None):
+        """experts: sequence of E coli_expert (device pointers); shared: coli_expert or None."""
+        arr = (coli_expert * len(experts))(*experts)
+        sh = ctypes.byref(shared) if shared is not None else None
+        _check(lib().colibri_moe_bind_experts(self.handle, arr, sh))
+
+    bind_experts = colibri_moe_bind_experts
+
+    def colibri_moe_forward(self, T: int, x, router_w, bias, out, workspace, workspace_bytes: int | None = None,
+                            residual=None, stream=None):
+        wb = self.workspace_bytes if workspace_bytes is None else workspace_bytes
+        _check(lib().colibri_moe_forward(self.handle, T, _ptr(x), _ptr(router_w), _ptr(bias), _ptr(residual),
+                                         _ptr(out), _ptr(workspace), wb, _stream(stream)))
+
+    forward = colibri_moe_forward
+
+    def colibri_moe_debug_routing(self, workspace, T: int, topk_idx=None, topk_w=None, near_tie=None,
+                                  expert_offsets=None, pair_token=None, pair_slot=None, stream=None):
+        _check(lib().colibri_moe_debug_routing(self.handle, _ptr(workspace), T, _ptr(topk_idx), _ptr(topk_w),
+                                               _ptr(near_tie), _ptr(expert_offsets), _ptr(pair_token),
+                                               _ptr(pair_slot), _stream(stream)))
+
+    debug_routing = colibri_moe_debug_routing
+
+    def colibri_moe_check_status(self, workspace, stream=None) -> int:
+        v = ctypes.c_int32()
+        rc = lib().colibri_moe_check_status(self.handle, _ptr(workspace), ctypes.byref(v), _stream(stream))
+        if rc not in (COLI_OK, COLI_EDEVICE):
+            _check(rc)
+        return v.value
+
+    check_status = colibri_moe_check_status
+
+    def colibri_moe_profile_begin(self, max_calls: int):
+        _check(lib().colibri_moe_profile_begin(self.handle, max_calls))
+
+    profile_begin = colibri_moe_profile_begin
+
+    def colibri_moe_profile_end(self):
+        """Returns {kernel name: (total ms, launches)}."""
+        buf = (coli_kernel_time * 32)()
+        n = ctypes.c_int()
+        _check(lib().colibri_moe_profile_end(self.handle, buf, 32, ctypes.byref(n)))
+        return {buf[i].name.decode(): (buf[i].total_ms, buf[i].launches) for i in range(min(n.value, 32))}
+
+    profile_end = colibri_moe_profile_end
+
+    def colibri_moe_last_launch_count(self) -> int:
+        return lib().colibri_moe_last_launch_count(self.handle)
+
+    last_launch_count = colibri_moe_last_launch_count
+
+    def close(self):
+        if self.handle:
+            lib().colibri_moe_destroy(self.handle)
+            self.handle = None
+
+    colibri_moe_destroy = close
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,390 @@
+// C ABI of the quantized sparse MoE layer library: plan validation, expert
+// binding (TMA tensor maps + device descriptor table), the forward launch
+// sequence, routing debug copies, status read-back and per-kernel timing.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+using namespace coli;
+
+namespace {
+
+thread_local std::string g_err;
+
+coli_status fail(coli_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+coli_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(COLI_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+enum KernelId { K_ROUTER = 0, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_COUNT };
+const char* kKernelNames[K_COUNT] = {"router_logits", "router_topk",    "permute", "prep_xs",
+                                     "expert_gate_up", "expert_down", "combine"};
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+struct coli_moe_plan {
+  coli_moe_desc desc;
+  WsLayout ws;
+  int Fmax;
+  bool bound = false;
+  int device = -1;
+  int num_sms = 0;
+  DevExpert* d_experts = nullptr;
+  CUtensorMap* d_maps = nullptr;
+  // profiling
+  int prof_max_calls = 0;
+  int prof_calls = 0;
+  std::vector<cudaEvent_t> prof_events;  // 2 per kernel launch
+  std::vector<int> prof_kernel;          // kernel id per event pair
+  int last_launches = 0;
+};
+
+static int matrix_row_bytes(int qtype, int K) { return qtype == COLI_Q_INT4_G128 ? K / 2 : K; }
+
+extern "C" {
+
+const char* colibri_moe_last_error(void) { return g_err.c_str(); }
+
+coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, size_t* workspace_bytes) {
+  if (!desc || !plan || !workspace_bytes) return fail(COLI_EINVAL, "plan: null argument");
+  const coli_moe_desc& d = *desc;
+  if (d.T_max < 1 || d.d < 1 || d.d_ff < 1 || d.E < 1 || d.k < 1)
+    return fail(COLI_EINVAL, "plan: T_max, d, d_ff, E, k must be positive");
+  if (d.E > kMaxE) return fail(COLI_EUNSUPPORTED, "plan: E=%d exceeds %d", d.E, kMaxE);
+  if (d.k > d.E || d.k > kMaxK) return fail(COLI_EINVAL, "plan: need 1 <= k <= min(E, %d)", kMaxK);
+  if (d.qtype != COLI_Q_INT4_G128 && d.qtype != COLI_Q_INT8_PC) return fail(COLI_EUNSUPPORTED, "plan: unknown qtype");
+  if (d.xtype != COLI_X_BF16 && d.xtype != COLI_X_F32) return fail(COLI_EUNSUPPORTED, "plan: unknown xtype");
+  if (d.has_shared != 0 && d.has_shared != 1) return fail(COLI_EINVAL, "plan: has_shared must be 0 or 1");
+  if (d.has_shared && d.shared_d_ff < 1) return fail(COLI_EINVAL, "plan: shared_d_ff must be positive");
+  const int mult = d.qtype == COLI_Q_INT4_G128 ? 256 : 128;
+  if (d.d % mult || d.d_ff % mult || (d.has_shared && d.shared_d_ff % mult))
+    return fail(COLI_EUNSUPPORTED, "plan: d and FFN sizes must be multiples of %d for this qtype", mult);
+  if ((long long)d.T_max * d.k > (1LL << 30)) return fail(COLI_EUNSUPPORTED, "plan: T_max*k too large");
+  if (!(d.routed_scale == d.routed_scale)) return fail(COLI_EINVAL, "plan: routed_scale is NaN");
+
+  coli_moe_plan* p = new (std::nothrow) coli_moe_plan();
+  if (!p) return fail(COLI_EINVAL, "plan: out of host memory");
+  p->desc = d;
+  p->Fmax = d.has_shared && d.shared_d_ff > d.d_ff ? d.shared_d_ff : d.d_ff;
+  const size_t T = (size_t)d.T_max, k = (size_t)d.k, E = (size_t)d.E;
+  const size_t P = T * k, rows = P + (d.has_shared ? T : 0);
+  WsLayout& w = p->ws;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  w.status = take(64);
+  w.topk_idx = take(T * k * 4);
+  w.topk_w = take(T * k * 4);
+  w.near_tie = take(T * 4);
+  w.offsets = take((E + 2) * 4);
+  w.pair_token = take(rows * 4);
+  w.pair_slot = take(P * 4);
+  w.pair_of = take(P * 4);
+  w.unique = take((E + 1) * 4);
+  w.n_unique = take(16);
+  w.logits = take((size_t)kRouterKSplit * T * E * 4);
+  w.xs = take(T * (size_t)d.d * 4);
+  w.h = take(rows * (size_t)p->Fmax * 4);
+  w.y = take(rows * (size_t)d.d * 4);
+  w.total = off;
+  *workspace_bytes = off;
+  *plan = p;
+  return COLI_OK;
+}
+
+void colibri_moe_destroy(coli_moe_plan_t* plan) {
+  if (!plan) return;
+  if (plan->device >= 0) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != plan->device) cudaSetDevice(plan->device);
+    cudaFree(plan->d_experts);
+    cudaFree(plan->d_maps);
+    for (cudaEvent_t e : plan->prof_events) cudaEventDestroy(e);
+    if (cur >= 0 && cur != plan->device) cudaSetDevice(cur);
+  }
+  delete plan;
+}
+
+coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* experts, const coli_expert* shared) {
+  if (!plan || !experts) return fail(COLI_EINVAL, "bind: null argument");
+  const coli_moe_desc& d = plan->desc;
+  if (d.has_shared && !shared) return fail(COLI_EINVAL, "bind: plan has a shared expert but shared is NULL");
+  if (!d.has_shared && shared) return fail(COLI_EINVAL, "bind: plan has no shared expert");
+  auto encode = get_encode();
+  if (!encode) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled is not available from the driver");
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "bind: cudaGetDevice");
+  int sms = 0;
+  ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "bind: cudaDeviceGetAttribute");
+
+  const int slots = d.E + (d.has_shared ? 1 : 0);
+  std::vector<DevExpert> hx((size_t)d.E + 1);
+  std::vector<CUtensorMap> hm(((size_t)d.E + 1) * 3);
+  memset(hx.data(), 0, hx.size() * sizeof(DevExpert));
+  memset(hm.data(), 0, hm.size() * sizeof(CUtensorMap));
+  const size_t sal = d.qtype == COLI_Q_INT4_G128 ? 2 : 4;
+  for (int s = 0; s < slots; ++s) {
+    const coli_expert& ex = s < d.E ? experts[s] : *shared;
+    const int F = s < d.E ? d.d_ff : d.shared_d_ff;
+    const coli_qmat* mats[3] = {&ex.gate, &ex.up, &ex.down};
+    for (int m = 0; m < 3; ++m) {
+      const coli_qmat& qm = *mats[m];
+      if (!qm.q || !qm.scale || !qm.zp) return fail(COLI_EINVAL, "bind: expert %d matrix %d has a null pointer", s, m);
+      if (!aligned(qm.q, 16)) return fail(COLI_EALIGN, "bind: expert %d matrix %d codes not 16-byte aligned", s, m);
+      if (!aligned(qm.scale, sal)) return fail(COLI_EALIGN, "bind: expert %d matrix %d scales misaligned", s, m);
+      const int N = m < 2 ? F : d.d, K = m < 2 ? d.d : F;
+      DevMat& dm = hx[s].m[m];
+      dm.q = static_cast<const uint8_t*>(qm.q);
+      dm.s = qm.scale;
+      dm.z = static_cast<const uint8_t*>(qm.zp);
+      dm.N = N;
+      dm.K = K;
+      const cuuint64_t row_bytes = (cuuint64_t)matrix_row_bytes(d.qtype, K);
+      const cuuint64_t gdim[2] = {row_bytes, (cuuint64_t)N};
+      const cuuint64_t gstride[1] = {row_bytes};
+      const cuuint32_t box[2] = {(cuuint32_t)kChunk, (cuuint32_t)(m < 2 ? kGateUpRows : kDownRows)};
+      const cuuint32_t estride[2] = {1, 1};
+      CUresult r = encode(&hm[(size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim,
+                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, s);
+    }
+    hx[s].F = F;
+  }
+  if (plan->device >= 0 && plan->device != dev)
+    return fail(COLI_ESTATE, "bind: plan was bound on device %d, current device is %d", plan->device, dev);
+  if (!plan->d_experts) {
+    ce = cudaMalloc(&plan->d_experts, hx.size() * sizeof(DevExpert));
+    if (ce != cudaSuccess) return cuda_fail(ce, "bind: cudaMalloc(descriptors)");
+    ce = cudaMalloc(&plan->d_maps, hm.size() * sizeof(CUtensorMap));
+    if (ce != cudaSuccess) return cuda_fail(ce, "bind: cudaMalloc(tensor maps)");
+  }
+  ce = cudaMemcpy(plan->d_experts, hx.data(), hx.size() * sizeof(DevExpert), cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) return cuda_fail(ce, "bind: upload descriptors");
+  ce = cudaMemcpy(plan->d_maps, hm.data(), hm.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
+  if (ce != cudaSuccess) return cuda_fail(ce, "bind: upload tensor maps");
+  plan->device = dev;
+  plan->num_sms = sms;
+  plan->bound = true;
+  return COLI_OK;
+}
+
+coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void* x, const float* router_w,
+                                const float* bias, const float* residual, float* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  coli_moe_plan_t* plan = const_cast<coli_moe_plan_t*>(plan_c);
+  if (!plan) return fail(COLI_EINVAL, "forward: null plan");
+  const coli_moe_desc& d = plan->desc;
+  if (!plan->bound) return fail(COLI_ESTATE, "forward: experts not bound (call colibri_moe_bind_experts)");
+  if (T < 1 || T > d.T_max) return fail(COLI_EINVAL, "forward: T=%d outside [1, %d]", T, d.T_max);
+  if (!x || !router_w || !bias || !out || !workspace) return fail(COLI_EINVAL, "forward: null pointer");
+  if (workspace_bytes < plan->ws.total)
+    return fail(COLI_EWORKSPACE, "forward: workspace %zu bytes < required %zu", workspace_bytes, plan->ws.total);
+  if (!aligned(workspace, 256)) return fail(COLI_EALIGN, "forward: workspace not 256-byte aligned");
+  if (!aligned(x, 16) || !aligned(router_w, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16)))
+    return fail(COLI_EALIGN, "forward: x, router_w, residual and out must be 16-byte aligned");
+  if (!aligned(bias, 4)) return fail(COLI_EALIGN, "forward: bias misaligned");
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const WsLayout& w = plan->ws;
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.experts = plan->d_experts;
+  a.maps = plan->d_maps;
+  a.T = T;
+  a.d = d.d;
+  a.F = d.d_ff;
+  a.Fs = d.has_shared ? d.shared_d_ff : 0;
+  a.E = d.E;
+  a.k = d.k;
+  a.qtype = d.qtype;
+  a.xtype = d.xtype;
+  a.has_shared = d.has_shared;
+  a.rho = d.routed_scale;
+  a.Fmax = plan->Fmax;
+  a.x = x;
+  a.router_w = router_w;
+  a.bias = bias;
+  a.residual = residual;
+  a.out = out;
+  a.status = reinterpret_cast<int32_t*>(ws + w.status);
+  a.topk_idx = reinterpret_cast<int32_t*>(ws + w.topk_idx);
+  a.topk_w = reinterpret_cast<float*>(ws + w.topk_w);
+  a.near_tie = reinterpret_cast<int32_t*>(ws + w.near_tie);
+  a.offsets = reinterpret_cast<int32_t*>(ws + w.offsets);
+  a.pair_token = reinterpret_cast<int32_t*>(ws + w.pair_token);
+  a.pair_slot = reinterpret_cast<int32_t*>(ws + w.pair_slot);
+  a.pair_of = reinterpret_cast<int32_t*>(ws + w.pair_of);
+  a.unique = reinterpret_cast<int32_t*>(ws + w.unique);
+  a.n_unique = reinterpret_cast<int32_t*>(ws + w.n_unique);
+  a.logits = reinterpret_cast<float*>(ws + w.logits);
+  a.xs = reinterpret_cast<float*>(ws + w.xs);
+  a.h = reinterpret_cast<float*>(ws + w.h);
+  a.y = reinterpret_cast<float*>(ws + w.y);
+
+  const bool prof = plan->prof_calls < plan->prof_max_calls;
+  int launches = 0;
+  auto run = [&](KernelId id, auto&& fn) -> cudaError_t {
+    if (prof) {
+      cudaEvent_t e0, e1;
+      cudaEventCreate(&e0);
+      cudaEventCreate(&e1);
+      cudaEventRecord(e0, st);
+      cudaError_t r = fn();
+      cudaEventRecord(e1, st);
+      plan->prof_events.push_back(e0);
+      plan->prof_events.push_back(e1);
+      plan->prof_kernel.push_back(id);
+      ++launches;
+      return r;
+    }
+    ++launches;
+    return fn();
+  };
+
+  cudaError_t ce = cudaMemsetAsync(ws + w.status, 0, 64, st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "forward: clear status");
+  if ((ce = run(K_ROUTER, [&] { return launch_router_logits(a, st); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: router_logits");
+  if ((ce = run(K_TOPK, [&] { return launch_router_topk(a, st); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: router_topk");
+  if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: permute");
+  if ((ce = run(K_PREP, [&] { return launch_prep_xs(a, st); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: prep_xs");
+  if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: expert_gate_up");
+  if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: expert_down");
+  if ((ce = run(K_COMBINE, [&] { return launch_combine(a, st); })) != cudaSuccess)
+    return cuda_fail(ce, "forward: combine");
+  plan->last_launches = launches;
+  if (prof) plan->prof_calls++;
+  return COLI_OK;
+}
+
+coli_status colibri_moe_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, void* stream) {
+  if (!h || !out) return fail(COLI_EINVAL, "rmsnorm: null pointer");
+  if (T < 1 || d < 4 || d % 4) return fail(COLI_EINVAL, "rmsnorm: need T >= 1 and d a positive multiple of 4");
+  if (!aligned(h, 16) || !aligned(out, 8)) return fail(COLI_EALIGN, "rmsnorm: h 16-byte, out 8-byte alignment");
+  if (!(eps >= 0.f)) return fail(COLI_EINVAL, "rmsnorm: eps must be >= 0");
+  cudaError_t ce = launch_rmsnorm_bf16(h, T, d, eps, out, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? COLI_OK : cuda_fail(ce, "rmsnorm");
+}
+
+coli_status colibri_moe_debug_routing(const coli_moe_plan_t* plan, const void* workspace, int T, int32_t* topk_idx,
+                                      float* topk_w, int32_t* near_tie, int32_t* expert_offsets, int32_t* pair_token,
+                                      int32_t* pair_slot, void* stream) {
+  if (!plan || !workspace) return fail(COLI_EINVAL, "debug_routing: null argument");
+  if (T < 1 || T > plan->desc.T_max) return fail(COLI_EINVAL, "debug_routing: bad T");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const WsLayout& w = plan->ws;
+  const size_t k = plan->desc.k;
+  struct Cp { void* dst; size_t off; size_t bytes; } cps[] = {
+      {topk_idx, w.topk_idx, T * k * 4}, {topk_w, w.topk_w, T * k * 4},       {near_tie, w.near_tie, (size_t)T * 4},
+      {expert_offsets, w.offsets, ((size_t)plan->desc.E + 1) * 4},            {pair_token, w.pair_token, T * k * 4},
+      {pair_slot, w.pair_slot, T * k * 4}};
+  for (const Cp& c : cps) {
+    if (!c.dst) continue;
+    cudaError_t ce = cudaMemcpyAsync(c.dst, ws + c.off, c.bytes, cudaMemcpyDefault, st);
+    if (ce != cudaSuccess) return cuda_fail(ce, "debug_routing: copy");
+  }
+  return COLI_OK;
+}
+
+coli_status colibri_moe_check_status(const coli_moe_plan_t* plan, const void* workspace, int32_t* device_status,
+                                     void* stream) {
+  if (!plan || !workspace || !device_status) return fail(COLI_EINVAL, "check_status: null argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t ce =
+      cudaMemcpyAsync(&v, static_cast<const uint8_t*>(workspace) + plan->ws.status, 4, cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "check_status");
+  *device_status = v;
+  if (v) return fail(COLI_EDEVICE, "device status 0x%x (bad expert id = 1, wait timeout = 2)", v);
+  return COLI_OK;
+}
+
+coli_status colibri_moe_profile_begin(coli_moe_plan_t* plan, int max_calls) {
+  if (!plan || max_calls < 0) return fail(COLI_EINVAL, "profile_begin: bad argument");
+  for (cudaEvent_t e : plan->prof_events) cudaEventDestroy(e);
+  plan->prof_events.clear();
+  plan->prof_kernel.clear();
+  plan->prof_calls = 0;
+  plan->prof_max_calls = max_calls;
+  return COLI_OK;
+}
+
+coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out, int max_kernels, int* n_kernels) {
+  if (!plan || (!out && max_kernels > 0) || !n_kernels) return fail(COLI_EINVAL, "profile_end: bad argument");
+  double tot[K_COUNT] = {0};
+  int cnt[K_COUNT] = {0};
+  coli_status rc = COLI_OK;
+  for (size_t i = 0; i < plan->prof_kernel.size(); ++i) {
+    cudaEvent_t e0 = plan->prof_events[2 * i], e1 = plan->prof_events[2 * i + 1];
+    float ms = 0.f;
+    cudaError_t ce = cudaEventSynchronize(e1);
+    if (ce == cudaSuccess) ce = cudaEventElapsedTime(&ms, e0, e1);
+    if (ce != cudaSuccess && rc == COLI_OK) rc = cuda_fail(ce, "profile_end");
+    tot[plan->prof_kernel[i]] += ms;
+    cnt[plan->prof_kernel[i]] += 1;
+  }
+  int n = 0;
+  for (int kid = 0; kid < K_COUNT; ++kid) {
+    if (!cnt[kid]) continue;
+    if (n < max_kernels) out[n] = coli_kernel_time{kKernelNames[kid], tot[kid], cnt[kid]};
+    ++n;
+  }
+  *n_kernels = n;
+  for (cudaEvent_t e : plan->prof_events) cudaEventDestroy(e);
+  plan->prof_events.clear();
+  plan->prof_kernel.clear();
+  plan->prof_max_calls = 0;
+  plan->prof_calls = 0;
+  return rc;
+}
+
+int colibri_moe_last_launch_count(const coli_moe_plan_t* plan) { return plan ? plan->last_launches : 0; }
+
+}  // extern "C"

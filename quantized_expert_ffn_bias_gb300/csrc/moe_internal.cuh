@@ -1,0 +1,226 @@
+// Internal definitions shared by the kernels and the C-ABI layer of the
+// quantized sparse MoE layer library.  sm_103a only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/colibri_moe.h"
+
+namespace coli {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kDecodeMaxT = 8;          // tokens per forward served by the dequant-GEMV kernels
+constexpr float kNearTie = 1e-5f;       // k-th minus (k+1)-th selection score below this = near-tie
+constexpr int kRouterKSplit = 4;        // K-splits of the router logits (partial sums summed in order)
+
+// ---------------------------------------------------------------- device tables
+
+// One expert's three packed matrices (device pointers) and sizes.
+struct DevMat {
+  const uint8_t* q;
+  const void* s;
+  const uint8_t* z;
+  int N, K;
+};
+struct DevExpert {
+  DevMat m[3];  // 0 gate [F][d], 1 up [F][d], 2 down [d][F]
+  int F;
+  int pad_;
+};
+
+// TMA boxes of the decode (dequant-GEMV) kernels: 128-byte column chunks of
+// 16 rows (gate/up) or 32 rows (down), 128-byte swizzled in shared memory.
+constexpr int kGateUpRows = 16;
+constexpr int kDownRows = 32;
+constexpr int kChunk = 128;              // bytes per TMA box row
+constexpr int kStageChunks = 2;          // 128-byte chunks per pipeline stage
+constexpr int kDecodeStages = 3;         // pipeline depth per warp
+constexpr int kDecodeWarps = 8;          // warps per CTA (each runs its own pipeline)
+
+// ---------------------------------------------------------------- workspace layout
+
+// Offsets (bytes) into the caller's workspace; computed by the plan.
+struct WsLayout {
+  size_t status;       // int32[16]: [0] status bits, [1] router last-CTA counter
+  size_t topk_idx;     // int32 [T_max][k]
+  size_t topk_w;       // float [T_max][k]
+  size_t near_tie;     // int32 [T_max]
+  size_t offsets;      // int32 [E+2]; offsets[E]..[E+1] = shared rows
+  size_t pair_token;   // int32 [P_max + T_max]
+  size_t pair_slot;    // int32 [P_max]
+  size_t pair_of;      // int32 [P_max]
+  size_t unique;       // int32 [E+1]
+  size_t n_unique;     // int32 [4]
+  size_t logits;       // float [kRouterKSplit][T_max][E]
+  size_t xs;           // float [min(T_max, kDecodeMaxT) or T_max][d]  (dequant-GEMV input, pre-scaled)
+  size_t h;            // float [P_max + T_max][Fmax]
+  size_t y;            // float [P_max + T_max][d]
+  size_t total;
+};
+
+// Everything a kernel needs to know about one forward call.
+struct FwdArgs {
+  const DevExpert* experts;   // [E+1], slot E = shared
+  const CUtensorMap* maps;    // [(E+1)*3]
+  int T, d, F, Fs, E, k, qtype, xtype, has_shared;
+  float rho;
+  int Fmax;                   // row stride of h
+  const void* x;
+  const float* router_w;
+  const float* bias;
+  const float* residual;
+  float* out;
+  int32_t* status;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* near_tie;
+  int32_t* offsets;
+  int32_t* pair_token;
+  int32_t* pair_slot;
+  int32_t* pair_of;
+  int32_t* unique;
+  int32_t* n_unique;
+  float* logits;
+  float* xs;
+  float* h;
+  float* y;
+};
+
+// ---------------------------------------------------------------- launchers (one .cu file each)
+
+cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
+cudaError_t launch_decode_down(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
+cudaError_t launch_combine(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, cudaStream_t st);
+
+// ---------------------------------------------------------------- device helpers
+
+#ifdef __CUDACC__
+
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // give up a pipeline wait after ~1 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier; false after ~1 s (the caller then
+// records COLI_DEV_WAIT_TIMEOUT and stops using the pipeline).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Make generic-proxy shared-memory accesses ordered before later async-proxy
+// (TMA / tensor core) accesses of this thread.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2D tiled TMA load into shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy for data read exactly once per call (streamed expert weights).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---- packed fp32x2 arithmetic (two lanes per instruction)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float4 ldg_nc_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int32_t bits) { atomicOr(status, bits); }
+
+#endif  // __CUDACC__
+
+}  // namespace coli

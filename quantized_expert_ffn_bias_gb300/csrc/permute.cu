@@ -1,0 +1,148 @@
+// Batch-union grouping ("25GB RAM runs 744B GLM-5.2" page (pwwt.cn),
+// section 3.4): the T*k (token, slot) pairs are grouped by expert so that each
+// chosen expert is streamed once for all of its tokens.  Deterministic:
+// counting sort by expert id, stable in the flat index t*k + j.
+//
+// Grid: one CTA per expert.  Every CTA builds the full histogram in shared
+// memory (the pair list is small and L2-resident), scans it, and scatters its
+// own expert's pairs with a block-wide ballot prefix.  CTA 0 also writes the
+// offsets, the list of experts that received tokens (ascending ids) and the
+// shared-expert rows.
+#include "moe_internal.cuh"
+
+namespace coli {
+
+constexpr int kPermThreads = 256;
+
+__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
+    if (lane == nw - 1) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(FwdArgs a) {
+  __shared__ int hist[kMaxE];
+  __shared__ int scan[kMaxE + 1];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int E = a.E, P = a.T * a.k, tid = threadIdx.x;
+  for (int e = tid; e < E; e += kPermThreads) hist[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < P; f += kPermThreads) {
+    const int e = a.topk_idx[f];
+    if (e < 0 || e >= E) set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
+    else atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  // exclusive scan over E bins, kPermThreads bins per round
+  int carry = 0;
+  for (int b = 0; b < E; b += kPermThreads) {
+    const int e = b + tid;
+    const int v = e < E ? hist[e] : 0;
+    const int ex = block_exclusive_scan(v, warp_tot, &total);
+    if (e < E) scan[e] = carry + ex;
+    carry += total;
+    __syncthreads();
+  }
+  if (tid == 0) scan[E] = carry;
+  __syncthreads();
+
+  const int me = blockIdx.x;
+  if (me < E && hist[me] > 0) {
+    int running = scan[me];
+    const int end = scan[me] + hist[me];
+    for (int f0 = 0; f0 < P && running < end; f0 += kPermThreads) {
+      const int f = f0 + tid;
+      const int m = (f < P && a.topk_idx[f] == me) ? 1 : 0;
+      const int ex = block_exclusive_scan(m, warp_tot, &total);
+      if (m) {
+        const int pos = running + ex;
+        a.pair_token[pos] = f / a.k;
+        a.pair_slot[pos] = f % a.k;
+        a.pair_of[f] = pos;
+      }
+      running += total;
+      __syncthreads();
+    }
+  }
+  if (blockIdx.x == 0) {
+    for (int e = tid; e <= E; e += kPermThreads) a.offsets[e] = scan[e];
+    if (tid == 0) a.offsets[E + 1] = P + (a.has_shared ? a.T : 0);
+    if (a.has_shared)
+      for (int t = tid; t < a.T; t += kPermThreads) a.pair_token[P + t] = t;
+    // experts with tokens, ascending
+    int ucarry = 0;
+    for (int b = 0; b < E; b += kPermThreads) {
+      const int e = b + tid;
+      const int f = (e < E && hist[e] > 0) ? 1 : 0;
+      const int ex = block_exclusive_scan(f, warp_tot, &total);
+      if (f) a.unique[ucarry + ex] = e;
+      ucarry += total;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      a.n_unique[0] = ucarry;
+      if (a.has_shared) a.unique[ucarry] = E;
+    }
+  }
+}
+
+cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st) {
+  permute_kernel<<<a.E, kPermThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ dequant-GEMV input
+// xs[t][k] = x[t][k] * 16^-p(k) (int4) or 256^-(k%2) (int8): the decode kernels
+// form (code - zero) * 16^p exactly from the code bits placed inside an fp32
+// mantissa, so the activation carries the inverse power of two (exact).
+__device__ __forceinline__ float pos_scale(int qtype, int k) {
+  if (qtype == COLI_Q_INT4_G128) {
+    const int r = k & 7;
+    const int p = r <= 4 ? r : r - 3;
+    return __uint_as_float((uint32_t)(127 - 4 * p) << 23);
+  }
+  return (k & 1) ? (1.0f / 256.0f) : 1.0f;
+}
+
+__global__ void prep_xs_kernel(FwdArgs a) {
+  const size_t n = (size_t)a.T * a.d;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int k = (int)(i % a.d);
+    float v;
+    if (a.xtype == COLI_X_BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16);
+    else v = static_cast<const float*>(a.x)[i];
+    a.xs[i] = v * pos_scale(a.qtype, k);
+  }
+}
+
+cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st) {
+  const size_t n = (size_t)a.T * a.d;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 1024) blocks = 1024;
+  prep_xs_kernel<<<blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace coli

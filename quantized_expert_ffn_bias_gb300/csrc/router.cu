@@ -1,0 +1,221 @@
+// Router: logits z = x Wr^T (fp32 FMA), s = sigmoid(z), u = s + bias, top-k by u
+// (ties -> lower expert id), gate weights g = rho * s / sum(s over the chosen).
+//
+// "25GB RAM runs 744B GLM-5.2" page (pwwt.cn), section 3.1 (sigmoid router,
+// 8 of 256) and section 4.3 (the balancing bias steers selection; routing,
+// selection and scaling must be reproduced exactly).  Logits stay in fp32 on
+// CUDA cores: a TF32 contraction would move scores by ~1e-3 and break exact
+// top-k agreement.
+#include "moe_internal.cuh"
+
+namespace coli {
+
+// ------------------------------------------------------------------ small-T GEMV
+// One warp per (expert, K-slice); partial logits [ks][t][e], summed in ks order
+// by the top-k kernel.
+template <int NT, int XT>
+__global__ void __launch_bounds__(256) router_gemv_kernel(FwdArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (gw >= a.E * kRouterKSplit) return;
+  const int e = gw / kRouterKSplit, ks = gw % kRouterKSplit;
+  const int L = a.d / kRouterKSplit;
+  const int k0 = ks * L;
+  const float* w = a.router_w + (size_t)e * a.d + k0;
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  for (int i = lane * 4; i < L; i += 128) {
+    const float4 wv = __ldg(reinterpret_cast<const float4*>(w + i));
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < a.T) {
+        float x0, x1, x2, x3;
+        if (XT == COLI_X_BF16) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(
+              static_cast<const uint16_t*>(a.x) + (size_t)t * a.d + k0 + i));
+          x0 = __uint_as_float(xv.x << 16);
+          x1 = __uint_as_float(xv.x & 0xFFFF0000u);
+          x2 = __uint_as_float(xv.y << 16);
+          x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+        } else {
+          const float4 xv = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * a.d + k0 + i));
+          x0 = xv.x; x1 = xv.y; x2 = xv.z; x3 = xv.w;
+        }
+        acc[t] = fmaf(x0, wv.x, acc[t]);
+        acc[t] = fmaf(x1, wv.y, acc[t]);
+        acc[t] = fmaf(x2, wv.z, acc[t]);
+        acc[t] = fmaf(x3, wv.w, acc[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    float v = acc[t];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0 && t < a.T) a.logits[((size_t)ks * a.T + t) * a.E + e] = v;
+  }
+}
+
+// ------------------------------------------------------------------ large-T tiled GEMM
+// C[t][e] over one K-split: 64x64 tile per CTA, 256 threads, 4x4 outputs each.
+constexpr int RB_M = 64, RB_N = 64, RB_K = 32;
+
+template <int XT>
+__global__ void __launch_bounds__(256) router_gemm_kernel(FwdArgs a) {
+  __shared__ float As[RB_K][RB_M + 4];
+  __shared__ float Bs[RB_K][RB_N + 4];
+  const int tid = threadIdx.x;
+  const int e0 = blockIdx.x * RB_N, t0 = blockIdx.y * RB_M, ks = blockIdx.z;
+  const int L = a.d / kRouterKSplit, kbeg = ks * L;
+  const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4x4 each
+  float acc[4][4] = {};
+  for (int kk = 0; kk < L; kk += RB_K) {
+    // load A (x) tile 64 x 32 and B (Wr) tile 64 x 32: 2048 elements each, 8 per thread
+    for (int i = tid; i < RB_M * RB_K; i += 256) {
+      const int r = i / RB_K, c = i % RB_K;
+      const int t = t0 + r, k = kbeg + kk + c;
+      float v = 0.f;
+      if (t < a.T) {
+        if (XT == COLI_X_BF16)
+          v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[(size_t)t * a.d + k] << 16);
+        else
+          v = static_cast<const float*>(a.x)[(size_t)t * a.d + k];
+      }
+      As[c][r] = v;
+      const int e = e0 + r;
+      Bs[c][r] = e < a.E ? a.router_w[(size_t)e * a.d + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int c = 0; c < RB_K; ++c) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[c][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[c][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= a.T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < a.E) a.logits[((size_t)ks * a.T + t) * a.E + e] = acc[i][j];
+    }
+  }
+}
+
+cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st) {
+  if (a.T <= kDecodeMaxT) {
+    const int warps = a.E * kRouterKSplit;
+    const int blocks = (warps + 7) / 8;
+#define COLI_GEMV(NT)                                                                           \
+  if (a.xtype == COLI_X_BF16) router_gemv_kernel<NT, COLI_X_BF16><<<blocks, 256, 0, st>>>(a);   \
+  else router_gemv_kernel<NT, COLI_X_F32><<<blocks, 256, 0, st>>>(a);
+    if (a.T <= 1) { COLI_GEMV(1) }
+    else if (a.T <= 2) { COLI_GEMV(2) }
+    else if (a.T <= 4) { COLI_GEMV(4) }
+    else { COLI_GEMV(8) }
+#undef COLI_GEMV
+  } else {
+    dim3 grid((a.E + RB_N - 1) / RB_N, (a.T + RB_M - 1) / RB_M, kRouterKSplit);
+    if (a.xtype == COLI_X_BF16) router_gemm_kernel<COLI_X_BF16><<<grid, 256, 0, st>>>(a);
+    else router_gemm_kernel<COLI_X_F32><<<grid, 256, 0, st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ top-k
+// One warp per token.  Shared memory per warp: u[E], s[E].
+constexpr int kTopkWarps = 4;
+
+__device__ __forceinline__ bool better(float ua, int ea, float ub, int eb) {
+  return ua > ub || (ua == ub && ea < eb);
+}
+
+__device__ __forceinline__ void warp_argmax(float& u, int& e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u2 = __shfl_xor_sync(0xffffffffu, u, o);
+    const int e2 = __shfl_xor_sync(0xffffffffu, e, o);
+    if (better(u2, e2, u, e)) { u = u2; e = e2; }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= a.T) return;
+  const int E = a.E, k = a.k;
+  float* u = sm + (size_t)warp * 2 * E;
+  float* s = u + E;
+  for (int e = lane; e < E; e += 32) {
+    float z = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < kRouterKSplit; ++ks) z += a.logits[((size_t)ks * a.T + t) * E + e];
+    const float sv = 1.0f / (1.0f + expf(-z));
+    s[e] = sv;
+    u[e] = sv + a.bias[e];
+  }
+  __syncwarp();
+  int my_sel = -1;          // lane j < k: the j-th pick (by u, descending)
+  float kth = 0.f;
+  for (int j = 0; j <= k && j < E; ++j) {
+    float bu = -INFINITY;
+    int be = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      const float v = u[e];
+      if (better(v, e, bu, be)) { bu = v; be = e; }
+    }
+    warp_argmax(bu, be);
+    if (j < k) {
+      if (lane == j) my_sel = be;
+      kth = bu;
+      if (lane == 0) u[be] = -INFINITY;
+      __syncwarp();
+    } else {
+      const float gap = kth - bu;
+      if (lane == 0) a.near_tie[t] = gap < kNearTie ? 1 : 0;
+    }
+  }
+  if (k >= E && lane == 0) a.near_tie[t] = 0;
+  // ascending expert-id order: rank of each pick among the picks
+  int rank = 0;
+  for (int i = 0; i < k; ++i) {
+    const int other = __shfl_sync(0xffffffffu, my_sel, i);
+    if (lane < k && other < my_sel) ++rank;
+  }
+  // lane r gets the r-th smallest id
+  int sorted_e = -1;
+  for (int i = 0; i < k; ++i) {
+    const int oe = __shfl_sync(0xffffffffu, my_sel, i);
+    const int orank = __shfl_sync(0xffffffffu, rank, i);
+    if (lane == orank) sorted_e = oe;
+  }
+  const float my_s = (lane < k) ? s[sorted_e] : 0.f;
+  float ssum = 0.f;  // sum in ascending id order
+  for (int i = 0; i < k; ++i) ssum += __shfl_sync(0xffffffffu, my_s, i);
+  if (lane < k) {
+    a.topk_idx[(size_t)t * k + lane] = sorted_e;
+    a.topk_w[(size_t)t * k + lane] = a.rho * my_s / ssum;
+  }
+}
+
+cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st) {
+  const int blocks = (a.T + kTopkWarps - 1) / kTopkWarps;
+  const size_t smem = (size_t)kTopkWarps * 2 * a.E * sizeof(float);
+  router_topk_kernel<<<blocks, kTopkWarps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace coli

@@ -1,0 +1,122 @@
+"""The five workloads at full size on the GPU vs the oracle (routing of every token, sampled outputs).
+
+Inputs follow the GLM-5.2-class shapes of the pages (d=7168, d_ff=2048, 256
+experts, top-8, int4 group-128 / int8 per-channel), seeded and synthetic.
+"""
+from __future__ import annotations
+
+import gc
+
+import numpy as np
+import pytest
+
+import harness as H
+import oracle as O
+from tests.gpu_parity import check_output, rel_l2, run_layer_parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import quantized_expert_ffn_bias_gb300 as coli
+    coli.build()
+    yield
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _sample(T, n, seed):
+    if T <= n:
+        return np.arange(T, dtype=np.int32)
+    return np.sort(np.random.default_rng(seed).choice(T, size=n, replace=False)).astype(np.int32)
+
+
+def _release(dl):
+    import torch
+    dl.close()
+    del dl
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_decode_T1_T4():
+    from harness.device import DeviceLayer
+    w = H.WORKLOADS["decode"]
+    layer = w.layer(0)
+    dl = DeviceLayer(layer, 4)
+    for T in (1, 4):
+        for stream in range(3):
+            x = w.x(T, stream)
+            rep = run_layer_parity(dl, layer, x)
+            print(f"decode T={T}: rel_l2={rep.rel_l2:.2e} max/rms={rep.max_abs_over_rms:.2e} near_ties={rep.near_ties}")
+    _release(dl)
+
+
+def test_mtp_verify_T3_shared_and_overlap():
+    from harness.device import DeviceLayer
+    w = H.WORKLOADS["mtp_verify"]
+    layer = w.layer(0)
+    dl = DeviceLayer(layer, 3)
+    overlaps = []
+    for stream in range(4):
+        x = w.x(3, stream)
+        rep = run_layer_parity(dl, layer, x)
+        idx = dl.routing(3)[0]
+        sets = [set(r) for r in idx]
+        overlaps += [len(sets[a] & sets[b]) / layer.k for a in range(3) for b in range(a + 1, 3)]
+        assert len(set().union(*sets)) < 3 * layer.k  # batch-union really merged something on average
+    print(f"mtp verify: mean pairwise expert overlap {np.mean(overlaps):.2f}")
+    _release(dl)
+
+
+def test_prefill_T2048_skewed():
+    from harness.device import DeviceLayer
+    w = H.WORKLOADS["prefill"]
+    layer = w.layer(0)
+    dl = DeviceLayer(layer, 2048)
+    x = w.x(2048, 0)
+    rep = run_layer_parity(dl, layer, x, tokens=_sample(2048, 48, 3))
+    off = dl.routing(2048)[3]
+    loads = np.diff(off)
+    print(f"prefill: loads min={loads.min()} max={loads.max()} idle={int((loads == 0).sum())} "
+          f"rel_l2={rep.rel_l2:.2e} near_ties={rep.near_ties}")
+    assert loads.max() > 400
+    _release(dl)
+
+
+def test_stacked_six_layers_T256():
+    """Six layers h <- h + MoE(bf16(RMSNorm(h))), alternating int4 / int8: each layer's GPU output
+    matches the oracle fed the GPU's own layer input; RMSNorm matches to one bf16 rounding."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+    w = H.WORKLOADS["stacked"]
+    T, eps = 256, w.rmsnorm_eps
+    x = w.x(T, 0)
+    h = to_dev(x, "cuda").view(torch.bfloat16).float().contiguous()
+    n = torch.empty((T, w.d), dtype=torch.int16, device="cuda")
+    toks = _sample(T, 24, 4)
+    for l in range(w.n_layers):
+        layer = w.layer(l)
+        dl = DeviceLayer(layer, T)
+        coli.colibri_moe_rmsnorm_bf16(h, T, w.d, eps, n, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        n_np = n.cpu().numpy().view(np.uint16)
+        h_np = h.cpu().numpy().astype(np.float64)
+        n_ref = O.bf16_bits_of(O.rmsnorm_bf16(h_np, eps))
+        diff = n_np != n_ref
+        assert diff.mean() < 1e-3, f"layer {l}: rmsnorm differs on {diff.sum()} elements"
+        if diff.any():
+            assert np.all(np.abs(n_np[diff].astype(np.int32) - n_ref[diff].astype(np.int32)) == 1)
+        rep = run_layer_parity(dl, layer, n_np, tokens=toks, residual=h_np.astype(np.float32))
+        print(f"stacked layer {l} ({'int4' if layer.qtype == 0 else 'int8'}): rel_l2={rep.rel_l2:.2e} "
+              f"near_ties={rep.near_ties}")
+        h_next = torch.empty_like(h)
+        dl.forward(n, out=h_next, residual=h)
+        torch.cuda.synchronize()
+        h = h_next
+        _release(dl)
