@@ -35,9 +35,9 @@ coli_status cuda_fail(cudaError_t e, const char* what) {
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum KernelId { K_ROUTER = 0, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_COUNT };
-const char* kKernelNames[K_COUNT] = {"router_logits", "router_topk",    "permute", "prep_xs",
-                                     "expert_gate_up", "expert_down", "combine"};
+enum KernelId { K_ROUTE = 0, K_ROUTER, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_COUNT };
+const char* kKernelNames[K_COUNT] = {"route_decode",   "router_logits", "router_topk", "permute",
+                                     "prep_xs",        "expert_gate_up", "expert_down", "combine"};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -180,10 +180,10 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
       const cuuint64_t row_bytes = (cuuint64_t)matrix_row_bytes(d.qtype, K);
       const cuuint64_t gdim[2] = {row_bytes, (cuuint64_t)N};
       const cuuint64_t gstride[1] = {row_bytes};
-      const cuuint32_t box[2] = {(cuuint32_t)kChunk, (cuuint32_t)(m < 2 ? kGateUpRows : kDownRows)};
+      const cuuint32_t box[2] = {(cuuint32_t)kTmaBoxBytes, (cuuint32_t)(m < 2 ? kGateUpBoxRows : kDownBoxRows)};
       const cuuint32_t estride[2] = {1, 1};
       CUresult r = encode(&hm[(size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim,
-                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, s);
     }
@@ -283,14 +283,19 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
 
   cudaError_t ce = cudaMemsetAsync(ws + w.status, 0, 64, st);
   if (ce != cudaSuccess) return cuda_fail(ce, "forward: clear status");
-  if ((ce = run(K_ROUTER, [&] { return launch_router_logits(a, st); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: router_logits");
-  if ((ce = run(K_TOPK, [&] { return launch_router_topk(a, st); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: router_topk");
-  if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: permute");
-  if ((ce = run(K_PREP, [&] { return launch_prep_xs(a, st); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: prep_xs");
+  if (T <= kDecodeMaxT) {
+    if ((ce = run(K_ROUTE, [&] { return launch_route_decode(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: route_decode");
+  } else {
+    if ((ce = run(K_ROUTER, [&] { return launch_router_logits(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: router_logits");
+    if ((ce = run(K_TOPK, [&] { return launch_router_topk(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: router_topk");
+    if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: permute");
+    if ((ce = run(K_PREP, [&] { return launch_prep_xs(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: prep_xs");
+  }
   if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
     return cuda_fail(ce, "forward: expert_gate_up");
   if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)

@@ -33,12 +33,11 @@ struct DevExpert {
   int pad_;
 };
 
-// TMA boxes of the decode (dequant-GEMV) kernels: 128-byte column chunks of
-// 16 rows (gate/up) or 32 rows (down), 128-byte swizzled in shared memory.
-constexpr int kGateUpRows = 16;
-constexpr int kDownRows = 32;
-constexpr int kChunk = 128;              // bytes per TMA box row
-constexpr int kStageChunks = 2;          // 128-byte chunks per pipeline stage
+// TMA boxes of the decode (dequant-GEMV) kernels: 256-byte column slices of
+// 8 rows (gate, up) or 16 rows (down), unswizzled.
+constexpr int kTmaBoxBytes = 256;
+constexpr int kGateUpBoxRows = 8;
+constexpr int kDownBoxRows = 16;
 constexpr int kDecodeStages = 3;         // pipeline depth per warp
 constexpr int kDecodeWarps = 8;          // warps per CTA (each runs its own pipeline)
 
@@ -93,6 +92,7 @@ struct FwdArgs {
 
 // ---------------------------------------------------------------- launchers (one .cu file each)
 
+cudaError_t launch_route_decode(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
@@ -220,6 +220,47 @@ __device__ __forceinline__ float4 ldg_nc_f4(const float* p) {
 }
 
 __device__ __forceinline__ void set_status(int32_t* status, int32_t bits) { atomicOr(status, bits); }
+
+// Block-wide exclusive prefix sum of one int per thread (blockDim.x a multiple
+// of 32, <= 1024).  *total receives the block sum.  Contains __syncthreads().
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < nw ? warp_tot[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
+    if (lane == nw - 1) *total = wi;
+  }
+  __syncthreads();
+  const int r = warp_tot[warp] + inc - v;
+  __syncthreads();
+  return r;
+}
+
+// Activation pre-scale for the dequant-GEMV at input index k: the kernels form
+// code * 16^p (int4, p = 0,1,2,3,4,2,3,4 for k mod 8) or code * 256^(k mod 2)
+// (int8) exactly, so the activation carries the inverse power of two (exact).
+__device__ __forceinline__ float act_prescale(int qtype, int k) {
+  if (qtype == COLI_Q_INT4_G128) {
+    const int r = k & 7;
+    const int p = r <= 4 ? r : r - 3;
+    return __uint_as_float((uint32_t)(127 - 4 * p) << 23);
+  }
+  return (k & 1) ? (1.0f / 256.0f) : 1.0f;
+}
 
 #endif  // __CUDACC__
 

@@ -14,33 +14,6 @@ namespace coli {
 
 constexpr int kPermThreads = 256;
 
-__device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int n = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += n;
-  }
-  if (lane == 31) warp_tot[warp] = inc;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < nw ? warp_tot[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    if (lane < nw) warp_tot[lane] = wi - w;  // exclusive warp offsets
-    if (lane == nw - 1) *total = wi;
-  }
-  __syncthreads();
-  const int r = warp_tot[warp] + inc - v;
-  __syncthreads();
-  return r;
-}
-
 __global__ void __launch_bounds__(kPermThreads) permute_kernel(FwdArgs a) {
   __shared__ int hist[kMaxE];
   __shared__ int scan[kMaxE + 1];
@@ -114,18 +87,7 @@ cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st) {
 }
 
 // ------------------------------------------------------------------ dequant-GEMV input
-// xs[t][k] = x[t][k] * 16^-p(k) (int4) or 256^-(k%2) (int8): the decode kernels
-// form (code - zero) * 16^p exactly from the code bits placed inside an fp32
-// mantissa, so the activation carries the inverse power of two (exact).
-__device__ __forceinline__ float pos_scale(int qtype, int k) {
-  if (qtype == COLI_Q_INT4_G128) {
-    const int r = k & 7;
-    const int p = r <= 4 ? r : r - 3;
-    return __uint_as_float((uint32_t)(127 - 4 * p) << 23);
-  }
-  return (k & 1) ? (1.0f / 256.0f) : 1.0f;
-}
-
+// xs[t][k] = x[t][k] * act_prescale(k), the activation of the dequant-GEMV kernels.
 __global__ void prep_xs_kernel(FwdArgs a) {
   const size_t n = (size_t)a.T * a.d;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
@@ -133,7 +95,7 @@ __global__ void prep_xs_kernel(FwdArgs a) {
     float v;
     if (a.xtype == COLI_X_BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16);
     else v = static_cast<const float*>(a.x)[i];
-    a.xs[i] = v * pos_scale(a.qtype, k);
+    a.xs[i] = v * act_prescale(a.qtype, k);
   }
 }
 

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(FwdArgs a) {
   float acc[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+#pragma unroll 4
   for (int i = lane * 4; i < L; i += 128) {
     const float4 wv = __ldg(reinterpret_cast<const float4*>(w + i));
 #pragma unroll
@@ -151,18 +152,14 @@ __device__ __forceinline__ void warp_argmax(float& u, int& e) {
   }
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a) {
-  extern __shared__ float sm[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTopkWarps + warp;
-  if (t >= a.T) return;
+// Top-k of one token by one warp.  u, s: this warp's shared scratch [E] each.
+__device__ void topk_token(const FwdArgs& a, int t, float* u, float* s) {
+  const int lane = threadIdx.x & 31;
   const int E = a.E, k = a.k;
-  float* u = sm + (size_t)warp * 2 * E;
-  float* s = u + E;
   for (int e = lane; e < E; e += 32) {
     float z = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < kRouterKSplit; ++ks) z += a.logits[((size_t)ks * a.T + t) * E + e];
+    for (int ks = 0; ks < kRouterKSplit; ++ks) z += __ldcg(a.logits + ((size_t)ks * a.T + t) * E + e);
     const float sv = 1.0f / (1.0f + expf(-z));
     s[e] = sv;
     u[e] = sv + a.bias[e];
@@ -195,7 +192,6 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a)
     const int other = __shfl_sync(0xffffffffu, my_sel, i);
     if (lane < k && other < my_sel) ++rank;
   }
-  // lane r gets the r-th smallest id
   int sorted_e = -1;
   for (int i = 0; i < k; ++i) {
     const int oe = __shfl_sync(0xffffffffu, my_sel, i);
@@ -209,12 +205,191 @@ __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a)
     a.topk_idx[(size_t)t * k + lane] = sorted_e;
     a.topk_w[(size_t)t * k + lane] = a.rho * my_s / ssum;
   }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a) {
+  extern __shared__ float sm[];
+  const int warp = threadIdx.x >> 5;
+  const int t = blockIdx.x * kTopkWarps + warp;
+  if (t >= a.T) return;
+  float* u = sm + (size_t)warp * 2 * a.E;
+  topk_token(a, t, u, u + a.E);
 }
 
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st) {
   const int blocks = (a.T + kTopkWarps - 1) / kTopkWarps;
   const size_t smem = (size_t)kTopkWarps * 2 * a.E * sizeof(float);
   router_topk_kernel<<<blocks, kTopkWarps * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fused decode routing (T <= 8)
+// One launch for the whole routing of a decode step:
+//   every CTA: its share of the activation pre-scaling (xs) and of the router
+//   GEMV (one warp per (expert, K-split), loads issued ahead of the FMAs);
+//   the last CTA to finish (atomic ticket on the workspace counter; no waiting)
+//   then runs top-k for every token and the batch-union grouping of the
+//   T*k <= 256 pairs.
+constexpr int kRouteThreads = 256;
+
+template <int NT, int XT>
+__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) {
+  extern __shared__ float sm[];            // last CTA: 8 warps x (u[E], s[E])
+  __shared__ int is_last;
+  __shared__ int hist[kMaxE];
+  __shared__ int scan[kMaxE + 1];
+  __shared__ int sidx[kDecodeMaxT * kMaxK];
+  __shared__ int warp_tot[32];
+  __shared__ int total;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  // (1) activation pre-scaling, grid-stride
+  {
+    const int n = a.T * a.d;
+    for (int i = blockIdx.x * kRouteThreads + tid; i < n; i += gridDim.x * kRouteThreads) {
+      const int k = i % a.d;
+      float v;
+      if (XT == COLI_X_BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16);
+      else v = static_cast<const float*>(a.x)[i];
+      a.xs[i] = v * act_prescale(a.qtype, k);
+    }
+  }
+  // (2) router GEMV partial logits
+  {
+    const int gw = (blockIdx.x * kRouteThreads + tid) >> 5;
+    if (gw < a.E * kRouterKSplit) {
+      const int e = gw / kRouterKSplit, ks = gw % kRouterKSplit;
+      const int L = a.d / kRouterKSplit, k0 = ks * L;
+      const float* w = a.router_w + (size_t)e * a.d + k0;
+      float acc[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+      constexpr int U = 4;
+      for (int base = lane * 4; base < L; base += 128 * U) {
+        float4 wv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = base + u * 128;
+          wv[u] = i < L ? __ldg(reinterpret_cast<const float4*>(w + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          if (t >= a.T) continue;
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            const int i = base + u * 128;
+            if (i >= L) continue;
+            float x0, x1, x2, x3;
+            if (XT == COLI_X_BF16) {
+              const uint2 xv = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) +
+                                                                    (size_t)t * a.d + k0 + i));
+              x0 = __uint_as_float(xv.x << 16);
+              x1 = __uint_as_float(xv.x & 0xFFFF0000u);
+              x2 = __uint_as_float(xv.y << 16);
+              x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+            } else {
+              const float4 xv =
+                  __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * a.d + k0 + i));
+              x0 = xv.x; x1 = xv.y; x2 = xv.z; x3 = xv.w;
+            }
+            acc[t] = fmaf(x0, wv[u].x, acc[t]);
+            acc[t] = fmaf(x1, wv[u].y, acc[t]);
+            acc[t] = fmaf(x2, wv[u].z, acc[t]);
+            acc[t] = fmaf(x3, wv[u].w, acc[t]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && t < a.T) a.logits[((size_t)ks * a.T + t) * a.E + e] = v;
+      }
+    }
+  }
+  // (3) ticket: the last CTA to arrive does the rest
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) is_last = (atomicAdd(a.status + 1, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // (4) top-k, one warp per token
+  {
+    const int warp = tid >> 5;
+    float* u = sm + (size_t)warp * 2 * a.E;
+    for (int t = warp; t < a.T; t += kRouteThreads / 32) topk_token(a, t, u, u + a.E);
+  }
+  __syncthreads();
+  // (5) grouping of the P = T*k pairs (stable counting sort by expert id)
+  const int E = a.E, P = a.T * a.k;
+  for (int e = tid; e < E; e += kRouteThreads) hist[e] = 0;
+  __syncthreads();
+  for (int f = tid; f < P; f += kRouteThreads) {
+    const int e = __ldcg(a.topk_idx + f);
+    sidx[f] = e;
+    if (e < 0 || e >= E) set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
+    else atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int b = 0; b < E; b += kRouteThreads) {
+    const int e = b + tid;
+    const int ex = block_exclusive_scan(e < E ? hist[e] : 0, warp_tot, &total);
+    if (e < E) scan[e] = carry + ex;
+    carry += total;
+  }
+  if (tid == 0) scan[E] = carry;
+  __syncthreads();
+  for (int f = tid; f < P; f += kRouteThreads) {
+    const int e = sidx[f];
+    if (e < 0 || e >= E) continue;
+    int rank = 0;
+    for (int g = 0; g < f; ++g) rank += sidx[g] == e;
+    const int pos = scan[e] + rank;
+    a.pair_token[pos] = f / a.k;
+    a.pair_slot[pos] = f % a.k;
+    a.pair_of[f] = pos;
+  }
+  for (int e = tid; e <= E; e += kRouteThreads) a.offsets[e] = scan[e];
+  if (tid == 0) a.offsets[E + 1] = P + (a.has_shared ? a.T : 0);
+  if (a.has_shared)
+    for (int t = tid; t < a.T; t += kRouteThreads) a.pair_token[P + t] = t;
+  int ucarry = 0;
+  for (int b = 0; b < E; b += kRouteThreads) {
+    const int e = b + tid;
+    const int fl = (e < E && hist[e] > 0) ? 1 : 0;
+    const int ex = block_exclusive_scan(fl, warp_tot, &total);
+    if (fl) a.unique[ucarry + ex] = e;
+    ucarry += total;
+  }
+  if (tid == 0) {
+    a.n_unique[0] = ucarry;
+    if (a.has_shared) a.unique[ucarry] = E;
+    a.status[1] = 0;
+  }
+}
+
+cudaError_t launch_route_decode(const FwdArgs& a, cudaStream_t st) {
+  const int warps = a.E * kRouterKSplit;
+  int blocks = (warps * 32 + kRouteThreads - 1) / kRouteThreads;
+  if (blocks < 1) blocks = 1;
+  const size_t smem = (size_t)(kRouteThreads / 32) * 2 * a.E * sizeof(float);
+#define COLI_ROUTE(NT)                                                                                    \
+  {                                                                                                       \
+    auto kern = a.xtype == COLI_X_BF16 ? route_decode_kernel<NT, COLI_X_BF16> : route_decode_kernel<NT, COLI_X_F32>; \
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);   \
+    if (e != cudaSuccess) return e;                                                                       \
+    kern<<<blocks, kRouteThreads, smem, st>>>(a);                                                         \
+  }
+  if (a.T <= 1) COLI_ROUTE(1)
+  else if (a.T <= 2) COLI_ROUTE(2)
+  else if (a.T <= 4) COLI_ROUTE(4)
+  else COLI_ROUTE(8)
+#undef COLI_ROUTE
   return cudaGetLastError();
 }
 
