@@ -119,7 +119,9 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.n_unique = take(16);
   w.logits = take((size_t)kRouterKSplit * T * E * 4);
   w.xs = take(T * (size_t)d.d * 4);
+  w.xsum = take(T * (size_t)(d.d / kXsumBlock) * 4);
   w.h = take(rows * (size_t)p->Fmax * 4);
+  w.hsum = take(rows * (size_t)(p->Fmax / 8) * 4);
   w.y = take(rows * (size_t)d.d * 4);
   w.total = off;
   *workspace_bytes = off;
@@ -180,7 +182,9 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
       const cuuint64_t row_bytes = (cuuint64_t)matrix_row_bytes(d.qtype, K);
       const cuuint64_t gdim[2] = {row_bytes, (cuuint64_t)N};
       const cuuint64_t gstride[1] = {row_bytes};
-      const cuuint32_t box[2] = {(cuuint32_t)kTmaBoxBytes, (cuuint32_t)(m < 2 ? kGateUpBoxRows : kDownBoxRows)};
+      // box width: 256 bytes, or the whole row when rows are shorter (128 bytes)
+      const cuuint32_t boxw = row_bytes < (cuuint64_t)kTmaBoxBytes ? (cuuint32_t)row_bytes : (cuuint32_t)kTmaBoxBytes;
+      const cuuint32_t box[2] = {boxw, (cuuint32_t)(m < 2 ? kGateUpBoxRows : kDownBoxRows)};
       const cuuint32_t estride[2] = {1, 1};
       CUresult r = encode(&hm[(size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim,
                           gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -258,7 +262,9 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   a.n_unique = reinterpret_cast<int32_t*>(ws + w.n_unique);
   a.logits = reinterpret_cast<float*>(ws + w.logits);
   a.xs = reinterpret_cast<float*>(ws + w.xs);
+  a.xsum = reinterpret_cast<float*>(ws + w.xsum);
   a.h = reinterpret_cast<float*>(ws + w.h);
+  a.hsum = reinterpret_cast<float*>(ws + w.hsum);
   a.y = reinterpret_cast<float*>(ws + w.y);
 
   const bool prof = plan->prof_calls < plan->prof_max_calls;

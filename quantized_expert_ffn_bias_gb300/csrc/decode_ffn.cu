@@ -5,49 +5,50 @@
 // (pwwt.cn), section 3.4) and dequantised as (code - zero_point) * scale
 // ("Colibri walkthrough" page (discosf.com), section 3.4).
 //
-// Work unit = one warp and 16 matrix rows: 8 rows of gate with the same 8
-// rows of up (SwiGLU needs both), or 16 rows of down.  A pipeline stage holds
-// 512 bytes of each of the 16 rows (TMA, two 256-byte boxes per row block);
-// lane l owns bytes [16l, 16l+16) of every row of the stage, i.e. 32 int4 or
-// 16 int8 codes.  The lane's activations for those codes are loaded once per
-// stage and reused for all 16 rows, and the 16 rows give 16 independent
-// accumulation chains.  After the last stage a butterfly reduction across the
-// 32 lanes leaves row r in lanes 2r and 2r+1.  Each warp runs its own
-// kDecodeStages-deep mbarrier pipeline.
+// Work unit = one warp and 16 matrix rows: 8 rows of gate with the same 8 rows
+// of up (SwiGLU needs both), or 16 rows of down.  A pipeline stage holds 512
+// bytes of each of the 16 rows (TMA boxes of 256 bytes); lane l owns bytes
+// [16l, 16l+16) of every row, i.e. 32 int4 or 16 int8 codes.  The lane's
+// activations are loaded once per stage (prefetched one stage ahead) and
+// reused for all 16 rows, which also give 16 independent accumulation chains.
+// A butterfly reduction across the warp ends the unit.  Each warp runs its own
+// kDecodeStages-deep mbarrier pipeline; every wait is bounded and a timeout
+// sets the workspace status word.
 //
 // Exact dequantisation in fp32: a code c placed at mantissa bit 4p (int4) or
 // 8p (int8) of the float 2^23 gives 2^23 + c*16^p; subtracting 2^23 leaves
 // c*16^p exactly, and the activation was pre-multiplied by 16^-p (an exact
-// power of two), so the product is c*x.  The zero-point is applied once per
-// (row, 32-code slice): sum((c - z) x) = sum(c x) - z sum(x).  Group sums are
-// scaled by the fp16 group scale (int4) or, at the end, by the row scale (int8).
+// power of two), so the product is c*x.  Per (row, group) the scale s and the
+// zero-point z enter once: s*sum((c - z) x) = s*sum(c x) - (s*z)*sum(x); the
+// (s, s*z) pairs of the stage's groups are built cooperatively in a 1 KB table
+// and sum(x) is precomputed per block of inputs.
 #include "moe_internal.cuh"
 
 namespace coli {
 
-constexpr int kUnitRows = 16;              // rows per warp unit (gate/up: 8 + 8)
-constexpr int kRowBytesPerStage = 512;     // bytes of each row per stage
-constexpr int kBoxBytes = kTmaBoxBytes;    // TMA box inner extent
-constexpr int kStageBytes = kUnitRows * kRowBytesPerStage;  // 8 KB
-constexpr float kMagic = 8388608.0f;       // 2^23
-constexpr uint32_t kMagicBits = 0x4B000000u;
+constexpr int kRows = 16;                                     // rows per warp unit
+constexpr int kRowBytesPerStage = 512;
+constexpr int kBoxBytes = kTmaBoxBytes;
+constexpr int kStageBytes = kRows * kRowBytesPerStage;        // 8 KB
+constexpr int kGroupsPerStage = 8;                            // int4: 1024 codes per row per stage
+constexpr int kMaxNT = 2;                                     // tokens per pass (more: further passes)
+
+static_assert(kGateUpBoxRows == kRows / 2 && kDownBoxRows == kRows, "TMA boxes must match the unit rows");
 
 struct Unit {
   int slot;   // expert slot (E = shared)
-  int rb;     // row block (8 rows of gate/up, or 16 rows of down)
+  int rb;     // row block: gate/up rows rb*8.., down rows rb*16..
   int pbeg;   // first grouped pair row of the expert
   int cnt;    // tokens routed to the expert
   int K;      // inputs of the streamed matrix
 };
 
-static_assert(kGateUpBoxRows == kUnitRows / 2 && kDownBoxRows == kUnitRows, "TMA boxes must match the unit rows");
-
 template <bool DOWN>
-__device__ __forceinline__ int rows_per_unit() { return DOWN ? kUnitRows : kUnitRows / 2; }
+__device__ __forceinline__ int block_rows() { return DOWN ? kRows : kRows / 2; }
 
 template <bool DOWN>
 __device__ __forceinline__ bool get_unit(const FwdArgs& a, int u, int n_routed, Unit& out) {
-  const int rows = rows_per_unit<DOWN>();
+  const int rows = block_rows<DOWN>();
   const int per_routed = (DOWN ? a.d : a.F) / rows;
   const int routed_units = n_routed * per_routed;
   int slot, rb;
@@ -64,14 +65,13 @@ __device__ __forceinline__ bool get_unit(const FwdArgs& a, int u, int n_routed, 
   out.rb = rb;
   out.pbeg = a.offsets[slot];
   out.cnt = a.offsets[slot + 1] - out.pbeg;
-  const int Fe = slot == a.E ? a.Fs : a.F;
-  out.K = DOWN ? Fe : a.d;
+  out.K = DOWN ? (slot == a.E ? a.Fs : a.F) : a.d;
   return true;
 }
 
 template <bool DOWN>
 __device__ __forceinline__ int n_units_of(const FwdArgs& a, int n_routed) {
-  const int rows = rows_per_unit<DOWN>();
+  const int rows = block_rows<DOWN>();
   const int per_routed = (DOWN ? a.d : a.F) / rows;
   const int per_shared = a.has_shared ? (DOWN ? a.d : a.Fs) / rows : 0;
   return n_routed * per_routed + per_shared;
@@ -80,18 +80,14 @@ __device__ __forceinline__ int n_units_of(const FwdArgs& a, int n_routed) {
 template <int QT>
 __device__ __forceinline__ int row_bytes_of(int K) { return QT == COLI_Q_INT4_G128 ? K / 2 : K; }
 
-// Cursor over this warp's (unit, pass, stage) sequence.
+// Cursor over a warp's (unit, pass, stage) sequence.
 struct Cursor {
-  int unit;
-  int pass;
-  int kb;
-  int n_kb;
-  int n_pass;
+  int unit, pass, kb, n_kb, n_pass;
   bool valid;
   Unit u;
 };
 
-template <int QT, bool DOWN, int NTMAX>
+template <int QT, bool DOWN>
 __device__ __forceinline__ void cursor_load(const FwdArgs& a, int n_routed, int n_units, int unit, Cursor& c) {
   c.unit = unit;
   c.pass = 0;
@@ -99,80 +95,155 @@ __device__ __forceinline__ void cursor_load(const FwdArgs& a, int n_routed, int 
   c.valid = unit < n_units && get_unit<DOWN>(a, unit, n_routed, c.u);
   if (c.valid) {
     c.n_kb = (row_bytes_of<QT>(c.u.K) + kRowBytesPerStage - 1) / kRowBytesPerStage;
-    c.n_pass = (c.u.cnt + NTMAX - 1) / NTMAX;
+    c.n_pass = (c.u.cnt + kMaxNT - 1) / kMaxNT;
     c.valid = c.n_pass > 0;
   }
 }
 
-template <int QT, bool DOWN, int NTMAX>
+template <int QT, bool DOWN>
 __device__ __forceinline__ void cursor_next(const FwdArgs& a, int n_routed, int n_units, int stride, Cursor& c) {
   if (++c.kb < c.n_kb) return;
   c.kb = 0;
   if (++c.pass < c.n_pass) return;
-  cursor_load<QT, DOWN, NTMAX>(a, n_routed, n_units, c.unit + stride, c);
+  cursor_load<QT, DOWN>(a, n_routed, n_units, c.unit + stride, c);
 }
 
-// TMA loads of one stage (lane 0): for each matrix, the unit's rows x up to
-// two 256-byte boxes.  Shared layout: [matrix][box half][rows][256 B].
+// Shared layout of a stage.  gate/up: [matrix][box][8 rows][boxw]; down: [box][16 rows][boxw]
+// (boxw = 256, or the row length for 128-byte rows).
+template <bool DOWN>
+__device__ __forceinline__ int stage_off(int r, int box, int boxw) {
+  return DOWN ? box * 4096 + r * boxw : (r >> 3) * 4096 + box * 2048 + (r & 7) * boxw;
+}
+
 template <int QT, bool DOWN>
 __device__ __forceinline__ void issue_stage(const FwdArgs& a, const Cursor& c, uint8_t* stage, uint64_t* bar,
                                             uint64_t policy) {
   const int rb_bytes = row_bytes_of<QT>(c.u.K);
+  const int boxw = rb_bytes < kBoxBytes ? rb_bytes : kBoxBytes;
   const int x0 = c.kb * kRowBytesPerStage;
   const int nbox = x0 + kBoxBytes < rb_bytes ? 2 : 1;
-  const int rows = rows_per_unit<DOWN>();
-  const int nmat = DOWN ? 1 : 2;
-  mbar_arrive_expect_tx(bar, (uint32_t)(nmat * nbox * rows * kBoxBytes));
-  for (int m = 0; m < nmat; ++m) {
-    const CUtensorMap* map = a.maps + (size_t)c.u.slot * 3 + (DOWN ? 2 : m);
-    for (int h = 0; h < nbox; ++h)
-      tma_load_2d(stage + (m * 2 + h) * rows * kBoxBytes, map, x0 + h * kBoxBytes, c.u.rb * rows, bar, policy);
+  mbar_arrive_expect_tx(bar, (uint32_t)(kRows * nbox * boxw));
+  if (DOWN) {
+    const CUtensorMap* map = a.maps + (size_t)c.u.slot * 3 + 2;
+    for (int b = 0; b < nbox; ++b)
+      tma_load_2d(stage + stage_off<true>(0, b, boxw), map, x0 + b * kBoxBytes, c.u.rb * kRows, bar, policy);
+  } else {
+    for (int m = 0; m < 2; ++m) {
+      const CUtensorMap* map = a.maps + (size_t)c.u.slot * 3 + m;
+      for (int b = 0; b < nbox; ++b)
+        tma_load_2d(stage + stage_off<false>(m * 8, b, boxw), map, x0 + b * kBoxBytes, c.u.rb * 8, bar, policy);
+    }
   }
 }
 
-__device__ __forceinline__ float f16_bits_to_float(uint16_t b) { return __half2float(__ushort_as_half(b)); }
-
-// position scales 16^p of the int4 codes of one 32-bit word (p = 0,1,2,3,4,2,3,4)
-__device__ __forceinline__ float int4_pos_scale(int i) {
-  const int r = i & 7;
-  const int p = r <= 4 ? r : r - 3;
-  return __uint_as_float((uint32_t)(127 + 4 * p) << 23);
+__device__ __forceinline__ float f16_bits_to_float(uint32_t b) {
+  return __half2float(__ushort_as_half((unsigned short)b));
 }
 
-// sum over one 32-bit word of int4 codes of c * x'  (x' pre-scaled), packed
-__device__ __forceinline__ float2 dot_word_int4(uint32_t q, const float* xp, float2 acc) {
-  const uint32_t v = q >> 12;
-  const float2 M2 = make_float2(kMagic, kMagic);
-  const float2 d01 = fsub2(make_float2(__uint_as_float((q & 0x0000000Fu) | kMagicBits),
-                                       __uint_as_float((q & 0x000000F0u) | kMagicBits)), M2);
-  const float2 d23 = fsub2(make_float2(__uint_as_float((q & 0x00000F00u) | kMagicBits),
-                                       __uint_as_float((q & 0x0000F000u) | kMagicBits)), M2);
-  const float2 d45 = fsub2(make_float2(__uint_as_float((q & 0x000F0000u) | kMagicBits),
-                                       __uint_as_float((v & 0x00000F00u) | kMagicBits)), M2);
-  const float2 d67 = fsub2(make_float2(__uint_as_float((v & 0x0000F000u) | kMagicBits),
-                                       __uint_as_float((v & 0x000F0000u) | kMagicBits)), M2);
-  acc = ffma2(d01, make_float2(xp[0], xp[1]), acc);
-  acc = ffma2(d23, make_float2(xp[2], xp[3]), acc);
-  acc = ffma2(d45, make_float2(xp[4], xp[5]), acc);
-  acc = ffma2(d67, make_float2(xp[6], xp[7]), acc);
+// The packed dequant-dot of one 32-bit word of int4 codes (PTX text): codes at
+// mantissa positions, minus the magic pair %M, times four activation pairs.
+#define COLI_WORD4(Q, X01, X23, X45, X67, M, FIRST)                       \
+  "shr.b32 v, " Q ", 12;\n\t"                                             \
+  "lop3.b32 a0, " Q ", 0x0000000F, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a1, " Q ", 0x000000F0, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a2, " Q ", 0x00000F00, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a3, " Q ", 0x0000F000, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a4, " Q ", 0x000F0000, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a5, v, 0x00000F00, 0x4B000000, 0xEA;\n\t"                     \
+  "lop3.b32 a6, v, 0x0000F000, 0x4B000000, 0xEA;\n\t"                     \
+  "lop3.b32 a7, v, 0x000F0000, 0x4B000000, 0xEA;\n\t"                     \
+  "mov.b64 p0, {a0, a1};\n\tmov.b64 p1, {a2, a3};\n\t"                    \
+  "mov.b64 p2, {a4, a5};\n\tmov.b64 p3, {a6, a7};\n\t"                    \
+  "sub.rn.f32x2 p0, p0, " M ";\n\tsub.rn.f32x2 p1, p1, " M ";\n\t"        \
+  "sub.rn.f32x2 p2, p2, " M ";\n\tsub.rn.f32x2 p3, p3, " M ";\n\t"        \
+  FIRST                                                                   \
+  "fma.rn.f32x2 %0, p1, " X23 ", %0;\n\t"                                 \
+  "fma.rn.f32x2 %0, p2, " X45 ", %0;\n\t"                                 \
+  "fma.rn.f32x2 %0, p3, " X67 ", %0;\n\t"
+
+#define COLI_WORD8(Q, X01, X23, M, FIRST)                                 \
+  "shr.b32 v, " Q ", 16;\n\t"                                             \
+  "lop3.b32 a0, " Q ", 0x000000FF, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a1, " Q ", 0x0000FF00, 0x4B000000, 0xEA;\n\t"                 \
+  "lop3.b32 a2, v, 0x000000FF, 0x4B000000, 0xEA;\n\t"                     \
+  "lop3.b32 a3, v, 0x0000FF00, 0x4B000000, 0xEA;\n\t"                     \
+  "mov.b64 p0, {a0, a1};\n\tmov.b64 p1, {a2, a3};\n\t"                    \
+  "sub.rn.f32x2 p0, p0, " M ";\n\tsub.rn.f32x2 p1, p1, " M ";\n\t"        \
+  FIRST                                                                   \
+  "fma.rn.f32x2 %0, p1, " X23 ", %0;\n\t"
+
+// One row slice: 32 int4 codes (a 16-byte piece) against the lane's 32
+// pre-scaled activations (16 pairs), as a packed fp32 pair.  m2 = (2^23, 2^23).
+__device__ __forceinline__ uint64_t dot_row_int4(uint4 w, const ulonglong2 (&x)[8], uint64_t m2) {
+  uint64_t acc;
+  asm("{\n\t"
+      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 p0, p1, p2, p3;\n\t"
+      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "mul.rn.f32x2 %0, p0, %3;\n\t")
+      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
+      "}"
+      : "=l"(acc)
+      : "r"(w.x), "r"(w.y), "l"(x[0].x), "l"(x[0].y), "l"(x[1].x), "l"(x[1].y), "l"(x[2].x), "l"(x[2].y),
+        "l"(x[3].x), "l"(x[3].y), "l"(m2));
+#ifdef COLI_SPLIT_CHAIN
+  // words 2..3 in a second, independent chain (halves the dependent FMA chain)
+  uint64_t acc2;
+  asm("{\n\t"
+      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 p0, p1, p2, p3;\n\t"
+      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "mul.rn.f32x2 %0, p0, %3;\n\t")
+      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
+      "}"
+      : "=l"(acc2)
+      : "r"(w.z), "r"(w.w), "l"(x[4].x), "l"(x[4].y), "l"(x[5].x), "l"(x[5].y), "l"(x[6].x), "l"(x[6].y),
+        "l"(x[7].x), "l"(x[7].y), "l"(m2));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(acc2));
+#else
+  asm("{\n\t"
+      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
+      ".reg .b64 p0, p1, p2, p3;\n\t"
+      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "fma.rn.f32x2 %0, p0, %3, %0;\n\t")
+      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
+      "}"
+      : "+l"(acc)
+      : "r"(w.z), "r"(w.w), "l"(x[4].x), "l"(x[4].y), "l"(x[5].x), "l"(x[5].y), "l"(x[6].x), "l"(x[6].y),
+        "l"(x[7].x), "l"(x[7].y), "l"(m2));
+#endif
   return acc;
 }
 
-__device__ __forceinline__ float2 dot_word_int8(uint32_t q, const float* xp, float2 acc) {
-  const uint32_t v = q >> 16;
-  const float2 M2 = make_float2(kMagic, kMagic);
-  const float2 d01 = fsub2(make_float2(__uint_as_float((q & 0x00FFu) | kMagicBits),
-                                       __uint_as_float((q & 0xFF00u) | kMagicBits)), M2);
-  const float2 d23 = fsub2(make_float2(__uint_as_float((v & 0x00FFu) | kMagicBits),
-                                       __uint_as_float((v & 0xFF00u) | kMagicBits)), M2);
-  acc = ffma2(d01, make_float2(xp[0], xp[1]), acc);
-  acc = ffma2(d23, make_float2(xp[2], xp[3]), acc);
+// One row slice of 16 int8 codes against 16 pre-scaled activations (8 pairs).
+__device__ __forceinline__ uint64_t dot_row_int8(uint4 w, const ulonglong2 (&x)[8], uint64_t m2) {
+  uint64_t acc;
+  asm("{\n\t"
+      ".reg .b32 v, a0, a1, a2, a3;\n\t"
+      ".reg .b64 p0, p1;\n\t"
+      COLI_WORD8("%1", "%5", "%6", "%13", "mul.rn.f32x2 %0, p0, %5;\n\t")
+      COLI_WORD8("%2", "%7", "%8", "%13", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
+      COLI_WORD8("%3", "%9", "%10", "%13", "fma.rn.f32x2 %0, p0, %9, %0;\n\t")
+      COLI_WORD8("%4", "%11", "%12", "%13", "fma.rn.f32x2 %0, p0, %11, %0;\n\t")
+      "}"
+      : "=l"(acc)
+      : "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w), "l"(x[0].x), "l"(x[0].y), "l"(x[1].x), "l"(x[1].y), "l"(x[2].x),
+        "l"(x[2].y), "l"(x[3].x), "l"(x[3].y), "l"(m2));
   return acc;
+}
+#undef COLI_WORD4
+#undef COLI_WORD8
+
+__device__ __forceinline__ float pair_sum(uint64_t p) {
+  return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
+}
+
+__device__ __forceinline__ ulonglong2 ldg_nc_u64x2(const float* p) {
+  ulonglong2 v;
+  asm volatile("ld.global.nc.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p));
+  return v;
 }
 
 // Butterfly reduction of v[16] across the warp: afterwards v[0] of lane l is
 // the warp-wide sum of row l >> 1.
-__device__ __forceinline__ float reduce16(float (&v)[kUnitRows]) {
+__device__ __forceinline__ float reduce16(float (&v)[kRows]) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -205,112 +276,170 @@ __device__ __forceinline__ float reduce16(float (&v)[kUnitRows]) {
   return v[0];
 }
 
-// Pre-scale of an activation feeding the next dequant-GEMV at input index k.
-template <int QT>
-__device__ __forceinline__ float pos_scale_inv(int k) {
-  if (QT == COLI_Q_INT4_G128) {
-    const int r = k & 7;
-    const int p = r <= 4 ? r : r - 3;
-    return __uint_as_float((uint32_t)(127 - 4 * p) << 23);
-  }
-  return (k & 1) ? (1.0f / 256.0f) : 1.0f;
+// row r of the unit -> (matrix, matrix row)
+template <bool DOWN>
+__device__ __forceinline__ void unit_row(const Unit& u, int r, int& mat, int& row) {
+  if (DOWN) { mat = 2; row = u.rb * kRows + r; }
+  else { mat = r >> 3; row = u.rb * 8 + (r & 7); }
 }
 
-// ------------------------------------------------------------------ one pass (nt tokens, all stages)
+// Raw (scale, zero-point) data of one stage for the (row, 4 groups) a lane fills
+// in the stage table: lane l covers row l >> 1 and groups 4*(l & 1) .. +3.
+struct ScaleRaw {
+  uint32_t s01, s23;   // four fp16 scales
+  uint32_t z4;         // four zero nibbles in the low 16 bits
+};
 
-template <int QT, bool DOWN, int NT, int NTMAX>
+template <bool DOWN>
+__device__ __forceinline__ ScaleRaw load_scales_int4(const DevExpert& ex, const Unit& u, int kb, int G) {
+  const int lane = threadIdx.x & 31;
+  const int r = lane >> 1;
+  const int g0 = kb * kGroupsPerStage + 4 * (lane & 1);
+  int mat, row;
+  unit_row<DOWN>(u, r, mat, row);
+  const DevMat& M = ex.m[mat];
+  const uint16_t* s = static_cast<const uint16_t*>(M.s) + (size_t)row * G + g0;
+  const uint8_t* z = M.z + (size_t)row * ((G + 1) / 2) + g0 / 2;
+  ScaleRaw o;
+  uint32_t sv[4], zv[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sv[i] = g0 + i < G ? __ldg(s + i) : 0u;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) zv[i] = g0 + 2 * i < G ? __ldg(z + i) : 0u;
+  o.s01 = sv[0] | (sv[1] << 16);
+  o.s23 = sv[2] | (sv[3] << 16);
+  o.z4 = zv[0] | (zv[1] << 8);
+  return o;
+}
+
+// Write the lane's four (s, s*z) entries of the stage table [16 rows][8 groups].
+__device__ __forceinline__ void store_scales_int4(float2* tab, const ScaleRaw& o) {
+  const int lane = threadIdx.x & 31;
+  float2* dst = tab + (lane >> 1) * kGroupsPerStage + 4 * (lane & 1);
+  const uint32_t sv[4] = {o.s01 & 0xFFFFu, o.s01 >> 16, o.s23 & 0xFFFFu, o.s23 >> 16};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float s = f16_bits_to_float(sv[i]);
+    const float z = (float)((o.z4 >> (4 * i)) & 15u);
+    dst[i] = make_float2(s, s * z);
+  }
+}
+
+// ------------------------------------------------------------------ one pass (NT tokens, all stages)
+
+template <int QT, bool DOWN, int NT>
 __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_units, int stride, const Cursor& cons,
-                                         Cursor& prod, uint8_t* wbuf, uint64_t* bars, int& stage, uint32_t& phase,
-                                         uint64_t policy) {
+                                         Cursor& prod, uint8_t* wbuf, uint64_t* bars, float2* tab, int& stage,
+                                         uint32_t& phase, uint64_t policy) {
   constexpr bool I4 = QT == COLI_Q_INT4_G128;
   constexpr int CODES = I4 ? 32 : 16;   // codes per lane per row per stage
+  constexpr int XQ = CODES / 4;         // 16-byte activation loads per token
   const int lane = threadIdx.x & 31;
-  const int rows = rows_per_unit<DOWN>();
   const Unit u = cons.u;
   const DevExpert& ex = a.experts[u.slot];
   const int rbytes = row_bytes_of<QT>(u.K);
-  const int G = u.K / 128, ZB = (G + 1) / 2;
+  const int boxw = rbytes < kBoxBytes ? rbytes : kBoxBytes;
+  const int G = u.K / 128;
 
-  // this pass's tokens (input rows)
-  const int p0 = u.pbeg + cons.pass * NTMAX;
-  const int ntok = min(NT, u.cnt - cons.pass * NTMAX);
+  // this pass's input rows and their block sums
+  const int p0 = u.pbeg + cons.pass * kMaxNT;
+  const int ntok = min(NT, u.cnt - cons.pass * kMaxNT);
   const float* xrow[NT];
+  const float* srow[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int tt = t < ntok ? t : 0;
-    xrow[t] = DOWN ? a.h + (size_t)(p0 + tt) * a.Fmax : a.xs + (size_t)a.pair_token[p0 + tt] * a.d;
+    if (DOWN) {
+      xrow[t] = a.h + (size_t)(p0 + tt) * a.Fmax;
+      srow[t] = a.hsum + (size_t)(p0 + tt) * (a.Fmax / 8);
+    } else {
+      const int tok = a.pair_token[p0 + tt];
+      xrow[t] = a.xs + (size_t)tok * a.d;
+      srow[t] = a.xsum + (size_t)tok * (a.d / kXsumBlock);
+    }
   }
-  // row r of the unit: gate/up rows rb*8 + (r & 7) of matrix r >> 3, or down row rb*16 + r
-  float acc[NT][kUnitRows];
+  auto code0_of = [&](int kb) {
+    const int kbyte = kb * kRowBytesPerStage + lane * 16;
+    return kbyte < rbytes ? (I4 ? kbyte * 2 : kbyte) : -1;
+  };
+  auto load_x = [&](int t, int code0, ulonglong2 (&xq)[8], float& xsum) {
+    const int c = code0 < 0 ? 0 : code0;
+#pragma unroll
+    for (int i = 0; i < XQ; ++i) xq[i] = ldg_nc_u64x2(xrow[t] + c + 4 * i);
+    if (DOWN) {          // sums of h over 8 consecutive inputs
+      if (I4) {
+        const float4 h4 = __ldg(reinterpret_cast<const float4*>(srow[t] + c / 8));
+        xsum = (h4.x + h4.y) + (h4.z + h4.w);
+      } else {
+        const float2 h2 = __ldg(reinterpret_cast<const float2*>(srow[t] + c / 8));
+        xsum = h2.x + h2.y;
+      }
+    } else {             // sums of x over blocks of 16 inputs
+      if (I4) {
+        const float2 s2 = __ldg(reinterpret_cast<const float2*>(srow[t] + c / kXsumBlock));
+        xsum = s2.x + s2.y;
+      } else {
+        xsum = __ldg(srow[t] + c / kXsumBlock);
+      }
+    }
+  };
+
+  // int8: the (s, s*z) of the unit's 16 rows, once per pass
+  if (!I4) {
+    __syncwarp();
+    if (lane < kRows) {
+      int mat, row;
+      unit_row<DOWN>(u, lane, mat, row);
+      const float s = __ldg(static_cast<const float*>(ex.m[mat].s) + row);
+      tab[lane] = make_float2(s, s * (float)__ldg(ex.m[mat].z + row));
+    }
+    __syncwarp();
+  }
+
+  float acc[NT][kRows];
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
-    for (int r = 0; r < kUnitRows; ++r) acc[t][r] = 0.f;
-  // int8: per-row zero-points (applied per stage) and scales (applied at the end)
-  float z8[kUnitRows];
-  if (!I4) {
-#pragma unroll
-    for (int r = 0; r < kUnitRows; ++r) {
-      const int mat = DOWN ? 2 : (r >> 3);
-      const int row = DOWN ? u.rb * kUnitRows + r : u.rb * 8 + (r & 7);
-      z8[r] = (float)__ldg(ex.m[mat].z + row);
-    }
-  }
+    for (int r = 0; r < kRows; ++r) acc[t][r] = 0.f;
+
+  const uint64_t m2 = 0x4B0000004B000000ull;   // (2^23, 2^23)
+  // prefetch for stage 0: activations of the first token, scales
+  ulonglong2 xq0[8];
+  float xs0 = 0.f;
+  load_x(0, code0_of(0), xq0, xs0);
+  ScaleRaw sr = {0u, 0u, 0u};
+  if (I4) sr = load_scales_int4<DOWN>(ex, u, 0, G);
 
   bool ok = true;
   for (int kb = 0; kb < cons.n_kb; ++kb) {
-    uint64_t* bar = bars + stage;
-    const int kbyte = kb * kRowBytesPerStage + lane * 16;   // this lane's 16 bytes of each row
-    const bool valid = kbyte < rbytes;
-    const int code0 = I4 ? kbyte * 2 : kbyte;
-    // scales / zero-points of the lane's group for the unit's rows (int4)
-    float sc[kUnitRows], zc[kUnitRows];
-    if constexpr (I4) {
-      const int g = valid ? code0 / 128 : 0;
-#pragma unroll
-      for (int r = 0; r < kUnitRows; ++r) {
-        const int mat = DOWN ? 2 : (r >> 3);
-        const int row = DOWN ? u.rb * kUnitRows + r : u.rb * 8 + (r & 7);
-        sc[r] = f16_bits_to_float(__ldg(static_cast<const uint16_t*>(ex.m[mat].s) + (size_t)row * G + g));
-        const uint32_t zb = __ldg(ex.m[mat].z + (size_t)row * ZB + (g >> 1));
-        zc[r] = (float)((g & 1) ? (zb >> 4) : (zb & 15u));
-      }
+    const int code0 = code0_of(kb);
+    if (I4) {                       // stage table of (s, s*z)
+      __syncwarp();
+      store_scales_int4(tab, sr);
+      __syncwarp();
     }
-    if (!mbar_wait(bar, phase)) { ok = false; break; }
-    if (valid) {
-      const uint8_t* sbase = wbuf + stage * kStageBytes;
-      const int half = lane >> 4, off = (lane & 15) * 16;
+    // current-stage activations (token 0 prefetched); prefetch the next stage
+    ulonglong2 xq[8];
+    float xsum = xs0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xq[i] = xq0[i];
+    if (kb + 1 < cons.n_kb) {
+      load_x(0, code0_of(kb + 1), xq0, xs0);
+      if (I4) sr = load_scales_int4<DOWN>(ex, u, kb + 1, G);
+    }
+    const int g = I4 ? (code0 < 0 ? 0 : (code0 >> 7) - kb * kGroupsPerStage) : 0;
+    if (!mbar_wait(bars + stage, phase)) { ok = false; break; }
+    if (code0 >= 0) {
+      const uint8_t* sbase = wbuf + stage * kStageBytes + (lane & 15) * 16;
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        float xp[CODES];
+        if (t > 0) load_x(t, code0, xq, xsum);
 #pragma unroll
-        for (int i = 0; i < CODES; i += 4) {
-          const float4 v = ldg_nc_f4(xrow[t] + code0 + i);
-          xp[i] = v.x; xp[i + 1] = v.y; xp[i + 2] = v.z; xp[i + 3] = v.w;
-        }
-        float xsum = 0.f;   // sum of the unscaled activations of the lane's codes
-#pragma unroll
-        for (int i = 0; i < CODES; ++i)
-          xsum = fmaf(xp[i], I4 ? int4_pos_scale(i) : ((i & 1) ? 256.f : 1.f), xsum);
-#pragma unroll
-        for (int r = 0; r < kUnitRows; ++r) {
-          const int mat_slot = DOWN ? 0 : (r >> 3);
-          const int rr = DOWN ? r : (r & 7);
-          const uint4 w = lds128(smem_u32(sbase + (mat_slot * 2 + half) * rows * kBoxBytes + rr * kBoxBytes + off));
-          float2 d2 = make_float2(0.f, 0.f);
-          if constexpr (I4) {
-            d2 = dot_word_int4(w.x, xp + 0, d2);
-            d2 = dot_word_int4(w.y, xp + 8, d2);
-            d2 = dot_word_int4(w.z, xp + 16, d2);
-            d2 = dot_word_int4(w.w, xp + 24, d2);
-            acc[t][r] = fmaf(sc[r], fmaf(-zc[r], xsum, d2.x + d2.y), acc[t][r]);
-          } else {
-            d2 = dot_word_int8(w.x, xp + 0, d2);
-            d2 = dot_word_int8(w.y, xp + 4, d2);
-            d2 = dot_word_int8(w.z, xp + 8, d2);
-            d2 = dot_word_int8(w.w, xp + 12, d2);
-            acc[t][r] += fmaf(-z8[r], xsum, d2.x + d2.y);
-          }
+        for (int r = 0; r < kRows; ++r) {
+          const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
+          const float2 sz = I4 ? tab[r * kGroupsPerStage + g] : tab[r];
+          const uint64_t d2 = I4 ? dot_row_int4(w, xq, m2) : dot_row_int8(w, xq, m2);
+          acc[t][r] = fmaf(sz.x, pair_sum(d2), fmaf(-sz.y, xsum, acc[t][r]));
         }
       }
     }
@@ -318,9 +447,9 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
     if (prod.valid) {
       if (lane == 0) {
         fence_proxy_async_smem();
-        issue_stage<QT, DOWN>(a, prod, wbuf + stage * kStageBytes, bar, policy);
+        issue_stage<QT, DOWN>(a, prod, wbuf + stage * kStageBytes, bars + stage, policy);
       }
-      cursor_next<QT, DOWN, NTMAX>(a, n_routed, n_units, stride, prod);
+      cursor_next<QT, DOWN>(a, n_routed, n_units, stride, prod);
     }
     if (++stage == kDecodeStages) { stage = 0; phase ^= 1u; }
   }
@@ -328,23 +457,22 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
 
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    const float v = reduce16(acc[t]);            // lane l: row l >> 1 of the unit
-    const int r = lane >> 1;
+    const float v = reduce16(acc[t]);           // lane l: row l >> 1 of the unit
     if (DOWN) {
-      const int row = u.rb * kUnitRows + r;
-      float val = v;
-      if (!I4) val *= __ldg(static_cast<const float*>(ex.m[2].s) + row);
-      if ((lane & 1) == 0 && t < ntok) a.y[(size_t)(p0 + t) * a.d + row] = val;
+      const int row = u.rb * kRows + (lane >> 1);
+      if ((lane & 1) == 0 && t < ntok) a.y[(size_t)(p0 + t) * a.d + row] = v;
     } else {
-      // lanes 0..15 hold gate rows 0..7, lanes 16..31 the same up rows
-      const int row = u.rb * 8 + (r & 7);
-      float val = v;
-      if (!I4) val *= __ldg(static_cast<const float*>(ex.m[r >> 3].s) + row);
-      const float upv = __shfl_down_sync(0xffffffffu, val, 16);
-      if (lane < 16 && (lane & 1) == 0 && t < ntok) {
-        const float hv = val / (1.0f + expf(-val)) * upv;
-        a.h[(size_t)(p0 + t) * a.Fmax + row] = hv * pos_scale_inv<QT>(row);
-      }
+      // lanes 0..15: gate rows 0..7, lanes 16..31: the same up rows
+      const float up = __shfl_down_sync(0xffffffffu, v, 16);
+      const float hv = v / (1.0f + expf(-v)) * up;          // silu(gate) * up
+      float hs = hv;                                           // sum of the 8 rows (lanes 0, 2, .., 14)
+      hs += __shfl_xor_sync(0xffffffffu, hs, 2);
+      hs += __shfl_xor_sync(0xffffffffu, hs, 4);
+      hs += __shfl_xor_sync(0xffffffffu, hs, 8);
+      const int row = u.rb * 8 + (lane >> 1);
+      if (lane < 16 && (lane & 1) == 0 && t < ntok)
+        a.h[(size_t)(p0 + t) * a.Fmax + row] = hv * act_prescale(QT, row);
+      if (lane == 0 && t < ntok) a.hsum[(size_t)(p0 + t) * (a.Fmax / 8) + u.rb] = hs;
     }
   }
   return true;
@@ -354,10 +482,12 @@ template <int QT, bool DOWN, int NTMAX>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t bars_all[kDecodeWarps][kDecodeStages];
+  __shared__ float2 tabs[kDecodeWarps][kRows * kGroupsPerStage];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* wbuf = smem + (size_t)warp * kDecodeStages * kStageBytes;
   uint64_t* bars = bars_all[warp];
+  float2* tab = tabs[warp];
 
   const int n_routed = a.n_unique[0];
   const int n_units = n_units_of<DOWN>(a, n_routed);
@@ -373,37 +503,32 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   const uint64_t policy = l2_evict_first_policy();
 
   Cursor prod, cons;
-  cursor_load<QT, DOWN, NTMAX>(a, n_routed, n_units, first, prod);
+  cursor_load<QT, DOWN>(a, n_routed, n_units, first, prod);
   cons = prod;
   for (int s = 0; s < kDecodeStages && prod.valid; ++s) {
     if (lane == 0) issue_stage<QT, DOWN>(a, prod, wbuf + s * kStageBytes, bars + s, policy);
-    cursor_next<QT, DOWN, NTMAX>(a, n_routed, n_units, stride, prod);
+    cursor_next<QT, DOWN>(a, n_routed, n_units, stride, prod);
   }
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
   while (cons.valid && ok) {
-    const int ntok = min(NTMAX, cons.u.cnt - cons.pass * NTMAX);
+    const int ntok = min(kMaxNT, cons.u.cnt - cons.pass * kMaxNT);
     if (NTMAX == 1 || ntok <= 1)
-      ok = run_pass<QT, DOWN, 1, NTMAX>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, stage, phase, policy);
-    else if (NTMAX == 2 || ntok <= 2)
-      ok = run_pass<QT, DOWN, (NTMAX >= 2 ? 2 : 1), NTMAX>(a, n_routed, n_units, stride, cons, prod, wbuf, bars,
-                                                          stage, phase, policy);
+      ok = run_pass<QT, DOWN, 1>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab, stage, phase, policy);
     else
-      ok = run_pass<QT, DOWN, NTMAX, NTMAX>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, stage, phase,
-                                            policy);
+      ok = run_pass<QT, DOWN, (NTMAX >= 2 ? 2 : 1)>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab, stage,
+                                                   phase, policy);
     cons.kb = cons.n_kb - 1;
-    cursor_next<QT, DOWN, NTMAX>(a, n_routed, n_units, stride, cons);
+    cursor_next<QT, DOWN>(a, n_routed, n_units, stride, cons);
   }
   if (!ok) {
-    if (lane == 0) set_status(a.status, COLI_DEV_WAIT_TIMEOUT);
-    // drain: wait (bounded) for the stages still in flight before the CTA's
-    // shared memory can be released
-    for (int s = 0; s < kDecodeStages; ++s) {
-      const int st = (stage + s) % kDecodeStages;
-      const uint32_t ph = phase ^ ((stage + s) >= kDecodeStages ? 1u : 0u);
-      mbar_wait(bars + st, ph);
+    if (lane == 0) {
+      set_status(a.status, COLI_DEV_WAIT_TIMEOUT);
+      // drain: wait (bounded) for the stages that may still have a copy in flight
+      for (int s = 0; s < kDecodeStages; ++s) mbar_wait(bars + s, phase ^ (s < stage ? 1u : 0u));
     }
+    __syncwarp();
   }
 }
 
@@ -411,12 +536,8 @@ template <int QT, bool DOWN, int NTMAX>
 static cudaError_t launch_decode_t(const FwdArgs& a, cudaStream_t st, int num_sms) {
   const size_t smem = (size_t)kDecodeWarps * kDecodeStages * kStageBytes + 1024;
   auto kern = decode_ffn_kernel<QT, DOWN, NTMAX>;
-  static bool attr_set = false;   // per template instance
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
   kern<<<num_sms, kDecodeWarps * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
@@ -427,11 +548,8 @@ static cudaError_t launch_decode(const FwdArgs& a, int max_tok, cudaStream_t st,
   if (max_tok <= 1)
     return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 1>(a, st, num_sms)
               : launch_decode_t<COLI_Q_INT8_PC, DOWN, 1>(a, st, num_sms);
-  if (max_tok <= 2)
-    return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 2>(a, st, num_sms)
-              : launch_decode_t<COLI_Q_INT8_PC, DOWN, 2>(a, st, num_sms);
-  return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 4>(a, st, num_sms)
-            : launch_decode_t<COLI_Q_INT8_PC, DOWN, 4>(a, st, num_sms);
+  return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 2>(a, st, num_sms)
+            : launch_decode_t<COLI_Q_INT8_PC, DOWN, 2>(a, st, num_sms);
 }
 
 cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok, cudaStream_t st, int num_sms) {

@@ -38,8 +38,15 @@ struct DevExpert {
 constexpr int kTmaBoxBytes = 256;
 constexpr int kGateUpBoxRows = 8;
 constexpr int kDownBoxRows = 16;
-constexpr int kDecodeStages = 3;         // pipeline depth per warp
-constexpr int kDecodeWarps = 8;          // warps per CTA (each runs its own pipeline)
+#ifndef COLI_DECODE_STAGES
+#define COLI_DECODE_STAGES 3
+#endif
+#ifndef COLI_DECODE_WARPS
+#define COLI_DECODE_WARPS 8
+#endif
+constexpr int kDecodeStages = COLI_DECODE_STAGES;   // pipeline depth per warp
+constexpr int kDecodeWarps = COLI_DECODE_WARPS;     // warps per CTA, each with its own pipeline
+constexpr int kXsumBlock = 16;           // activation block sums are kept per 16 inputs
 
 // ---------------------------------------------------------------- workspace layout
 
@@ -56,8 +63,10 @@ struct WsLayout {
   size_t unique;       // int32 [E+1]
   size_t n_unique;     // int32 [4]
   size_t logits;       // float [kRouterKSplit][T_max][E]
-  size_t xs;           // float [min(T_max, kDecodeMaxT) or T_max][d]  (dequant-GEMV input, pre-scaled)
-  size_t h;            // float [P_max + T_max][Fmax]
+  size_t xs;           // float [T_max][d]  (dequant-GEMV input, pre-scaled)
+  size_t xsum;         // float [T_max][d / kXsumBlock]  (unscaled block sums of x)
+  size_t h;            // float [P_max + T_max][Fmax]  (pre-scaled SwiGLU output)
+  size_t hsum;         // float [P_max + T_max][Fmax / 8]  (unscaled sums of h over 8 rows)
   size_t y;            // float [P_max + T_max][d]
   size_t total;
 };
@@ -86,7 +95,9 @@ struct FwdArgs {
   int32_t* n_unique;
   float* logits;
   float* xs;
+  float* xsum;
   float* h;
+  float* hsum;
   float* y;
 };
 
@@ -130,6 +141,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
                "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {

@@ -97,6 +97,16 @@ __global__ void prep_xs_kernel(FwdArgs a) {
     else v = static_cast<const float*>(a.x)[i];
     a.xs[i] = v * act_prescale(a.qtype, k);
   }
+  const size_t nb = n / kXsumBlock;   // unscaled sums of x over blocks of 16 inputs
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nb; i += (size_t)gridDim.x * blockDim.x) {
+    float sum = 0.f;
+    for (int j = 0; j < kXsumBlock; ++j) {
+      const size_t e = i * kXsumBlock + j;
+      sum += a.xtype == COLI_X_BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[e] << 16)
+                                    : static_cast<const float*>(a.x)[e];
+    }
+    a.xsum[i] = sum;
+  }
 }
 
 cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st) {

@@ -254,6 +254,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
       else v = static_cast<const float*>(a.x)[i];
       a.xs[i] = v * act_prescale(a.qtype, k);
     }
+    const int nb = n / kXsumBlock;   // unscaled sums of x over blocks of 16 inputs
+    for (int i = blockIdx.x * kRouteThreads + tid; i < nb; i += gridDim.x * kRouteThreads) {
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kXsumBlock; ++j) {
+        const int e = i * kXsumBlock + j;
+        sum += XT == COLI_X_BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[e] << 16)
+                                 : static_cast<const float*>(a.x)[e];
+      }
+      a.xsum[i] = sum;
+    }
   }
   // (2) router GEMV partial logits
   {
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
       float acc[NT];
 #pragma unroll
       for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-      constexpr int U = 4;
+      constexpr int U = 16;
       for (int base = lane * 4; base < L; base += 128 * U) {
         float4 wv[U];
 #pragma unroll
