@@ -157,6 +157,30 @@ COLI_API coli_status colibri_moe_forward(const coli_moe_plan_t* plan, int T, con
                                 size_t workspace_bytes, void* stream);
 
 /*
+ * The same forward pass with no workspace argument, for callers that cannot
+ * allocate device memory (a host framework that owns all allocations, or a
+ * region of code where allocating is not allowed).  There is no counterpart
+ * in the pages; this is an interface convenience.
+ *   The workspace is a fixed 8 MiB array in the library's device memory (every
+ *   GPU that loads the library holds it until the process exits).  Plans whose
+ *   workspace (colibri_moe_plan's *workspace_bytes) exceeds 8 MiB are refused
+ *   with COLI_EWORKSPACE; that covers decode-sized plans (GLM-class layer:
+ *   T_max up to about 16).
+ *   The first call on a device looks up the array's device address once
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture.  Nothing is allocated (no cudaMalloc or cudaFree).
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; each call clears what must start at zero.  Calls that overlap on
+ *   the GPU (different streams, or different host threads) race on the array
+ *   and must be serialised by the caller.  Refused (COLI_ESTATE) while
+ *   per-kernel profiling is active on the plan.
+ * Other arguments and errors as colibri_moe_forward.
+ */
+COLI_API coli_status colibri_moe_forward_noalloc(const coli_moe_plan_t* plan, int T, const void* x,
+                                                 const float* router_w, const float* bias, const float* residual,
+                                                 float* out, void* stream);
+
+/*
  * RMSNorm with unit gain, rounded to bf16 (the input of the next stacked
  * layer): out[t][i] = bf16(h[t][i] / sqrt(mean_i(h[t][i]^2) + eps)).
  * h device float [T][d]; out device uint16 (bf16 bits) [T][d]; d % 4 == 0.

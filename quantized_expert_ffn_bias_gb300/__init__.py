@@ -73,6 +73,8 @@ def lib():
             L.colibri_moe_bind_experts.restype = st
             L.colibri_moe_forward.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
             L.colibri_moe_forward.restype = st
+            L.colibri_moe_forward_noalloc.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+            L.colibri_moe_forward_noalloc.restype = st
             L.colibri_moe_rmsnorm_bf16.argtypes = [vp, i32, i32, ctypes.c_float, vp, vp]
             L.colibri_moe_rmsnorm_bf16.restype = st
             L.colibri_moe_debug_routing.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp]
@@ -154,6 +156,13 @@ class Plan:
                                          _ptr(out), _ptr(workspace), wb, _stream(stream)))
 
     forward = colibri_moe_forward
+
+    def colibri_moe_forward_noalloc(self, T: int, x, router_w, bias, out, residual=None, stream=None):
+        """Forward with the library's static scratch instead of a caller workspace (see the header)."""
+        _check(lib().colibri_moe_forward_noalloc(self.handle, T, _ptr(x), _ptr(router_w), _ptr(bias),
+                                                 _ptr(residual), _ptr(out), _stream(stream)))
+
+    forward_noalloc = colibri_moe_forward_noalloc
 
     def colibri_moe_debug_routing(self, workspace, T: int, topk_idx=None, topk_w=None, near_tie=None,
                                   expert_offsets=None, pair_token=None, pair_slot=None, stream=None):

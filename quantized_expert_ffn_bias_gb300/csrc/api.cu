@@ -399,3 +399,51 @@ coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out
 int colibri_moe_last_launch_count(const coli_moe_plan_t* plan) { return plan ? plan->last_launches : 0; }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ forward without caller workspace
+//
+// For callers that cannot allocate device memory at all: code running under a
+// host framework that owns every allocation, or inside a region where an
+// allocation is not allowed.  The workspace of the forward pass lives in a
+// fixed file-scope device array instead.  Its address is a device address
+// only when taken with cudaGetSymbolAddress on the device that uses it (the
+// array's name in host code is a host-side stand-in), so the first call on
+// each device looks it up once and caches it.
+
+namespace {
+constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB, held by every device that loads the library
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+constexpr int kNoAllocMaxDevices = 64;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+}  // namespace
+
+extern "C" coli_status colibri_moe_forward_noalloc(const coli_moe_plan_t* plan, int T, const void* x,
+                                                   const float* router_w, const float* bias, const float* residual,
+                                                   float* out, void* stream) {
+  if (!plan) return fail(COLI_EINVAL, "forward_noalloc: null plan");
+  if (plan->ws.total > kNoAllocScratchBytes)
+    return fail(COLI_EWORKSPACE,
+                "forward_noalloc: this plan needs %zu bytes of workspace, more than the %zu-byte static scratch; "
+                "use a smaller T_max or colibri_moe_forward with a caller workspace",
+                plan->ws.total, kNoAllocScratchBytes);
+  if (plan->prof_calls < plan->prof_max_calls)
+    return fail(COLI_ESTATE, "forward_noalloc: per-kernel profiling is active on this plan (it creates events)");
+  int dev = -1;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "forward_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(COLI_EUNSUPPORTED, "forward_noalloc: device index %d", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      ce = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_scratch);
+      if (ce != cudaSuccess) {
+        g_noalloc_ptr[dev] = nullptr;
+        return cuda_fail(ce, "forward_noalloc: cudaGetSymbolAddress(scratch)");
+      }
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return colibri_moe_forward(plan, T, x, router_w, bias, residual, out, scratch, kNoAllocScratchBytes, stream);
+}
