@@ -35,9 +35,13 @@ coli_status cuda_fail(cudaError_t e, const char* what) {
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-enum KernelId { K_ROUTE = 0, K_ROUTER, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_COMBINE, K_COUNT };
-const char* kKernelNames[K_COUNT] = {"route_decode",   "router_logits", "router_topk", "permute",
-                                     "prep_xs",        "expert_gate_up", "expert_down", "combine"};
+enum KernelId {
+  K_ROUTE = 0, K_ROUTER, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_GATHER, K_TILES, K_TC_GATEUP, K_TC_DOWN,
+  K_COMBINE, K_COUNT
+};
+const char* kKernelNames[K_COUNT] = {"route_decode", "router_logits",  "router_topk",    "permute",
+                                     "prep_xs",      "expert_gate_up", "expert_down",    "gather_x",
+                                     "plan_tiles",   "tc_gate_up",     "tc_down",        "combine"};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -123,6 +127,15 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.h = take(rows * (size_t)p->Fmax * 4);
   w.hsum = take(rows * (size_t)(p->Fmax / 8) * 4);
   w.y = take(rows * (size_t)d.d * 4);
+  w.xh = w.chunks = w.gu_tiles = w.dn_tiles = w.pf_counts = 0;
+  if (d.T_max > kDecodeMaxT) {
+    const size_t max_chunks = (E + 1) + rows / kPrefillChunk + 2;
+    w.xh = take(rows * (size_t)d.d * 2);
+    w.chunks = take(max_chunks * 16);
+    w.gu_tiles = take(max_chunks * (size_t)(p->Fmax / kPrefillRows) * 16);
+    w.dn_tiles = take(max_chunks * (size_t)(d.d / kPrefillRows) * 16);
+    w.pf_counts = take(16);
+  }
   w.total = off;
   *workspace_bytes = off;
   *plan = p;
@@ -159,7 +172,7 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
 
   const int slots = d.E + (d.has_shared ? 1 : 0);
   std::vector<DevExpert> hx((size_t)d.E + 1);
-  std::vector<CUtensorMap> hm(((size_t)d.E + 1) * 3);
+  std::vector<CUtensorMap> hm(((size_t)d.E + 1) * 6);   // [0, 3(E+1)): dequant-GEMV boxes; then tensor-core boxes
   memset(hx.data(), 0, hx.size() * sizeof(DevExpert));
   memset(hm.data(), 0, hm.size() * sizeof(CUtensorMap));
   const size_t sal = d.qtype == COLI_Q_INT4_G128 ? 2 : 4;
@@ -190,6 +203,12 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
                           gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, s);
+      // tensor-core path: 64 codes (32 or 64 bytes) x 128 rows, unswizzled
+      const cuuint32_t box2[2] = {(cuuint32_t)(d.qtype == COLI_Q_INT4_G128 ? 32 : 64), (cuuint32_t)kPrefillRows};
+      r = encode(&hm[((size_t)d.E + 1) * 3 + (size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                 const_cast<void*>(qm.q), gdim, gstride, box2, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled (tensor-core box) failed (%d)", (int)r);
     }
     hx[s].F = F;
   }
@@ -299,13 +318,54 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
       return cuda_fail(ce, "forward: router_topk");
     if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: permute");
-    if ((ce = run(K_PREP, [&] { return launch_prep_xs(a, st); })) != cudaSuccess)
-      return cuda_fail(ce, "forward: prep_xs");
   }
-  if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: expert_gate_up");
-  if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)
-    return cuda_fail(ce, "forward: expert_down");
+  if (T <= kDecodeMaxT) {
+    if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: expert_gate_up");
+    if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: expert_down");
+  } else {
+    // tensor-core path: fp16 activations in grouped order, tile tables, two grouped GEMMs
+    const int rows = T * d.k + (d.has_shared ? T : 0);
+    __half* xh = reinterpret_cast<__half*>(ws + w.xh);
+    __half* hh = reinterpret_cast<__half*>(ws + w.h);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + w.pf_counts);
+    auto encode = get_encode();
+    if (!encode) return fail(COLI_ECUDA, "forward: cuTensorMapEncodeTiled is not available");
+    CUtensorMap xmap, hmap;
+    {
+      const cuuint64_t gdim[2] = {(cuuint64_t)d.d, (cuuint64_t)rows};
+      const cuuint64_t gstr[1] = {(cuuint64_t)d.d * 2};
+      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t es[2] = {1, 1};
+      CUresult r = encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, gdim, gstr, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "forward: activation tensor map (%d)", (int)r);
+      const cuuint64_t hdim[2] = {(cuuint64_t)plan->Fmax, (cuuint64_t)rows};
+      const cuuint64_t hstr[1] = {(cuuint64_t)plan->Fmax * 2};
+      r = encode(&hmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, hh, hdim, hstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "forward: hidden tensor map (%d)", (int)r);
+    }
+    const CUtensorMap* wmaps = plan->d_maps + ((size_t)d.E + 1) * 3;
+    if ((ce = run(K_GATHER, [&] { return launch_gather_x(a, xh, rows, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: gather_x");
+    if ((ce = run(K_TILES, [&] {
+           return launch_plan_tiles(a, ws + w.chunks, ws + w.gu_tiles, ws + w.dn_tiles, counts, st);
+         })) != cudaSuccess)
+      return cuda_fail(ce, "forward: plan_tiles");
+    if ((ce = run(K_TC_GATEUP, [&] {
+           return launch_prefill_gateup(a, ws + w.chunks, ws + w.gu_tiles, counts + 1, wmaps, xmap, hh, st,
+                                        plan->num_sms);
+         })) != cudaSuccess)
+      return cuda_fail(ce, "forward: tc_gate_up");
+    if ((ce = run(K_TC_DOWN, [&] {
+           return launch_prefill_down(a, ws + w.chunks, ws + w.dn_tiles, counts + 2, wmaps, hmap, a.y, st,
+                                      plan->num_sms);
+         })) != cudaSuccess)
+      return cuda_fail(ce, "forward: tc_down");
+  }
   if ((ce = run(K_COMBINE, [&] { return launch_combine(a, st); })) != cudaSuccess)
     return cuda_fail(ce, "forward: combine");
   plan->last_launches = launches;

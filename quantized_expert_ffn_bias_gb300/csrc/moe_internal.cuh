@@ -68,6 +68,12 @@ struct WsLayout {
   size_t h;            // float [P_max + T_max][Fmax]  (pre-scaled SwiGLU output)
   size_t hsum;         // float [P_max + T_max][Fmax / 8]  (unscaled sums of h over 8 rows)
   size_t y;            // float [P_max + T_max][d]
+  // tensor-core path (T_max > kDecodeMaxT only; 0 otherwise)
+  size_t xh;           // fp16 [P_max + T_max][d]  activations in grouped order
+  size_t chunks;       // chunk table (16 B each)
+  size_t gu_tiles;     // gate/up tile table (16 B each)
+  size_t dn_tiles;     // down tile table (16 B each)
+  size_t pf_counts;    // int32[4]: chunks, gate/up tiles, down tiles
   size_t total;
 };
 
@@ -112,6 +118,17 @@ cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok_per_expert, cudaS
 cudaError_t launch_decode_down(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_combine(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, cudaStream_t st);
+cudaError_t launch_gather_x(const FwdArgs& a, __half* xh, int rows, cudaStream_t st);
+cudaError_t launch_plan_tiles(const FwdArgs& a, void* chunks, void* gu_tiles, void* dn_tiles, int32_t* counts,
+                              cudaStream_t st);
+cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
+                                  const CUtensorMap* wmaps, const CUtensorMap& xmap, __half* hout, cudaStream_t st,
+                                  int num_sms);
+cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
+                                const CUtensorMap* wmaps, const CUtensorMap& hmap, float* yout, cudaStream_t st,
+                                int num_sms);
+constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box height of the raw-code maps)
+constexpr int kPrefillChunk = 256;  // tokens per chunk
 
 // ---------------------------------------------------------------- device helpers
 
