@@ -203,11 +203,16 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
                           gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, s);
-      // tensor-core path: 64 codes (32 or 64 bytes) x 128 rows, unswizzled
-      const cuuint32_t box2[2] = {(cuuint32_t)(d.qtype == COLI_Q_INT4_G128 ? 32 : 64), (cuuint32_t)kPrefillRows};
+      // tensor-core path: one pipeline stage of codes (32, 64 or 128 bytes) x 128 rows, stored with
+      // the swizzle of the same width so that the dequantising threads read rows without bank conflicts
+      const int pf_row = prefill_raw_row_bytes(d.qtype, m < 2);
+      const cuuint32_t box2[2] = {(cuuint32_t)pf_row, (cuuint32_t)kPrefillRows};
+      const CUtensorMapSwizzle swz = pf_row == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                     : pf_row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                    : CU_TENSOR_MAP_SWIZZLE_128B;
       r = encode(&hm[((size_t)d.E + 1) * 3 + (size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                 const_cast<void*>(qm.q), gdim, gstride, box2, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                 const_cast<void*>(qm.q), gdim, gstride, box2, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled (tensor-core box) failed (%d)", (int)r);
     }
     hx[s].F = F;

@@ -128,7 +128,15 @@ cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void
                                 const CUtensorMap* wmaps, const CUtensorMap& hmap, float* yout, cudaStream_t st,
                                 int num_sms);
 constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box height of the raw-code maps)
-constexpr int kPrefillChunk = 256;  // tokens per chunk
+constexpr int kPrefillChunk = 128;  // tokens per chunk (largest MMA N)
+
+// K extent of one pipeline stage of the tensor-core path: 64 for gate/up (two
+// matrices per stage), 128 for down, so that every stage dequantises 128 x 128
+// fp16 weights.  The raw-code TMA box of a matrix is one stage wide.
+__host__ __device__ constexpr int prefill_stage_k(bool gate_up) { return gate_up ? 64 : 128; }
+__host__ __device__ constexpr int prefill_raw_row_bytes(int qtype, bool gate_up) {
+  return qtype == COLI_Q_INT4_G128 ? prefill_stage_k(gate_up) / 2 : prefill_stage_k(gate_up);
+}
 
 // ---------------------------------------------------------------- device helpers
 
@@ -184,6 +192,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Non-blocking probe of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Spinning wait for the thread that issues tensor-core instructions: the MMA
+// stream stalls while that thread is busy, and a test_wait on a completed
+// phase returns several times faster than a try_wait.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
   }
 }
 

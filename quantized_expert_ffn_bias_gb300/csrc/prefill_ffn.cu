@@ -1,7 +1,7 @@
 // Expert FFN for large token counts (prefill, batched verification): grouped
 // GEMMs on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
 //
-// Each chosen expert's weights are dequantised once per chunk of up to 256 of
+// Each chosen expert's weights are dequantised once per chunk of up to 128 of
 // its tokens (batch-union grouping, "25GB RAM runs 744B GLM-5.2" page
 // (pwwt.cn), section 3.4) and multiplied with those tokens' activations:
 //   gate/up: D[n][t] = sum_k W[n][k] * X[t][k] for 128 weight rows n (MMA M =
@@ -15,29 +15,45 @@
 // exactly in fp16's normal range, and fp16 keeps 11 significant bits of the
 // dequantised weights where bf16 would keep 8.
 //
-// CTA (persistent, one per SM): warp 0 issues TMA loads (raw codes, activation
-// rows), warp 1 owns TMEM and issues the MMAs (one thread), warps 2..9
-// dequantise into 128-byte-swizzled K-major tiles and run the epilogue.  All
+// The dequantised weight tile is the MMA's A operand and lives in tensor
+// memory (written with tcgen05.st), so shared memory only carries the raw
+// codes and the activation tiles; with small N an A operand in shared memory
+// would be re-read by every MMA and shared-memory bandwidth would set the pace.
+//
+// int4 unpacking: a 32-bit word holds 8 codes n0..n7 (code i in bits 4i..4i+3).
+// Masking the word and its 4/8/12-bit shifts with 0x000F000F gives the pairs
+// (n0,n4), (n1,n5), (n2,n6), (n3,n7) in one logic op each, so within every
+// group of 8 inputs the A operand holds the codes in the order
+// 0,4,1,5,2,6,3,7.  The activation matrices (X for gate/up, H for down) are
+// stored with the same permutation inside each group of 8 columns, which
+// leaves every dot product unchanged.  int8 keeps the natural order.
+//
+// CTA (persistent, one per SM): warp 0 issues TMA loads (raw codes and
+// activation rows) into a ring of stages, with L2 prefetch of the codes further
+// ahead; warp 1 owns TMEM and issues the MMAs (one thread); warps 2..5 run the
+// epilogue; warps 6..21 dequantise into a 4-deep ring of TMEM A stages.  All
 // waits are bounded; a timeout sets the status word and every role stops.
 #include "moe_internal.cuh"
 
 namespace coli {
 
-constexpr int kPfM = 128;          // weight rows per tile (MMA M)
-constexpr int kPfN = 256;          // tokens per chunk (largest MMA N)
-constexpr int kPfKB = 64;          // K elements per stage (one 128-byte swizzle atom of fp16)
-constexpr int kPfBBox = 64;        // activation rows per TMA box
-constexpr int kPfDqWarps = 8;
-constexpr int kPfThreads = (2 + kPfDqWarps) * 32;
-constexpr int kPfABytes = kPfM * 128;      // 16 KB per matrix
-constexpr int kPfBBytes = kPfN * 128;      // 32 KB
+constexpr int kPfM = 128;           // weight rows per tile (MMA M, TMEM lanes)
+constexpr int kPfN = kPrefillChunk;  // tokens per chunk (largest MMA N)
+constexpr int kPfBBox = 64;         // activation rows per TMA box
+constexpr int kPfEpWarps = 4;       // epilogue warps (one per TMEM sub-partition)
+constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-partition)
+constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps) * 32;
+constexpr int kPfAStages = 4;       // TMEM A ring depth
 
 struct PfChunk { int slot, row0, ntok, pad; };
 struct PfTile { int chunk, mb, pad0, pad1; };
 
 // ------------------------------------------------------------------ activations -> fp16, grouped order
+// xh[r][8j + p] = x[pair_token[r]][8j + perm(p)], perm = 0,4,1,5,2,6,3,7 for
+// int4 weights (the order the int4 unpacking produces) and the identity for int8.
 __global__ void gather_x_f16_kernel(FwdArgs a, __half* xh, int rows) {
   const int per_row = a.d / 8;
+  const bool perm = a.qtype == COLI_Q_INT4_G128;
   const long long n = (long long)rows * per_row;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     const int r = (int)(i / per_row), c = (int)(i % per_row) * 8;
@@ -56,18 +72,19 @@ __global__ void gather_x_f16_kernel(FwdArgs a, __half* xh, int rows) {
       const float4 f0 = p[0], f1 = p[1];
       v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w; v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
     }
-    uint4 o;
-    o.x = __half_as_ushort(__float2half_rn(v[0])) | ((uint32_t)__half_as_ushort(__float2half_rn(v[1])) << 16);
-    o.y = __half_as_ushort(__float2half_rn(v[2])) | ((uint32_t)__half_as_ushort(__float2half_rn(v[3])) << 16);
-    o.z = __half_as_ushort(__float2half_rn(v[4])) | ((uint32_t)__half_as_ushort(__float2half_rn(v[5])) << 16);
-    o.w = __half_as_ushort(__float2half_rn(v[6])) | ((uint32_t)__half_as_ushort(__float2half_rn(v[7])) << 16);
-    *reinterpret_cast<uint4*>(xh + (size_t)r * a.d + c) = o;
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = perm ? v[j] : v[2 * j], hi = perm ? v[j + 4] : v[2 * j + 1];
+      o[j] = (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+    }
+    *reinterpret_cast<uint4*>(xh + (size_t)r * a.d + c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
 // ------------------------------------------------------------------ chunk and tile tables
 // One CTA: experts with tokens (ascending, shared last) are cut into chunks of
-// up to 256 tokens; every chunk yields one tile per 128 output rows.
+// up to kPfN tokens; every chunk yields one tile per 128 output rows.
 __global__ void __launch_bounds__(256) plan_tiles_kernel(FwdArgs a, PfChunk* chunks, PfTile* gu_tiles,
                                                          PfTile* dn_tiles, int32_t* counts) {
   __shared__ int warp_tot[32];
@@ -145,11 +162,49 @@ __device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// The eight K16 MMAs of one pipeline stage in one block: the issuing thread
+// is on the critical path of the tensor pipe, so it executes as few
+// instructions per MMA as possible.  `kb` is the stage's index within the
+// tile: stage 0 overwrites the accumulators, later stages add to them.
+// gate/up: A stage = [gate K64 | up K64] (32 columns each), B = one 128-byte atom.
+__device__ __forceinline__ void umma_stage_gu(uint32_t d_gate, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a0, a1, a2, a3, a4, a5, a6, a7, dup;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+      "add.u32 dup, %0, 128;\n\t"
+      "add.u32 a1, %1, 32;\n\tadd.u32 a2, %1, 8;\n\tadd.u32 a3, %1, 40;\n\t"
+      "add.u32 a4, %1, 16;\n\tadd.u32 a5, %1, 48;\n\tadd.u32 a6, %1, 24;\n\tadd.u32 a7, %1, 56;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a3], b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a5], b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a7], b3, %3, q;\n\t}" ::"r"(d_gate),
+      "r"(a), "l"(b), "r"(idesc), "r"(kb));
+}
+// down: A stage = K128 (64 columns), B = two 128-byte atoms 16 * atom16 bytes apart.
+__device__ __forceinline__ void umma_stage_dn(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb,
+                                              uint32_t atom16) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7, bb;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
+      "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t"
+      "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"
+      "cvt.u64.u32 bb, %5;\n\t"
+      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
+      "add.u64 b4, %2, bb;\n\tadd.u64 b5, b4, 2;\n\tadd.u64 b6, b4, 4;\n\tadd.u64 b7, b4, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b4, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], b5, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b6, %3, q;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], b7, %3, q;\n\t}" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(kb), "r"(atom16));
 }
 
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -160,17 +215,26 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 16 consecutive TMEM columns of this warp's 32 lanes -> registers (issue only)
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// registers -> 16 consecutive TMEM columns of this warp's 32 lanes
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 2D TMA load without cache hint (activation rows: reused across the m-blocks of a chunk).
 __device__ __forceinline__ void tma_load_2d_nohint(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -181,15 +245,11 @@ __device__ __forceinline__ void tma_load_2d_nohint(void* dst, const CUtensorMap*
       : "memory");
 }
 
-// int4 -> fp16 pairs (1024 + code) in input order, see the file header
-__device__ __forceinline__ void int4_word_to_h1024(uint32_t q, uint32_t (&h)[4]) {
-  const uint32_t r = q >> 4;
-  const uint32_t v0 = __byte_perm(q, r, 0x5410);
-  const uint32_t v1 = __byte_perm(q, r, 0x7632);
-  h[0] = (v0 & 0x000F000Fu) | 0x64006400u;
-  h[1] = ((v0 >> 8) & 0x000F000Fu) | 0x64006400u;
-  h[2] = (v1 & 0x000F000Fu) | 0x64006400u;
-  h[3] = ((v1 >> 8) & 0x000F000Fu) | 0x64006400u;
+// Prefetch a 2D box of a tensor into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
@@ -202,6 +262,15 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
+// fp16 pair (1024 + (x & 15), 1024 + ((x >> 16) & 15)): exact, one logic op
+__device__ __forceinline__ uint32_t nib2_h1024(uint32_t x) { return (x & 0x000F000Fu) | 0x64006400u; }
+
+// Physical 16-byte chunk of logical chunk c in row r of a TMA box with rows of
+// RB bytes stored with the RB-byte swizzle (RB = 32, 64 or 128).
+template <int RB>
+__device__ __forceinline__ int swz_chunk(int r, int c) {
+  return c ^ (((r * RB) >> 7) & (RB / 16 - 1));
+}
 
 // ------------------------------------------------------------------ the grouped GEMM
 
@@ -209,22 +278,32 @@ struct PfArgs {
   const PfChunk* chunks;
   const PfTile* tiles;
   const int32_t* n_tiles;      // device scalar
-  const CUtensorMap* wmaps;    // [(E+1)*3] raw-code maps (box: 64 codes x 128 rows)
-  __half* hout;                // gate/up: H [rows][Fmax] fp16
+  const CUtensorMap* wmaps;    // [(E+1)*3] raw-code maps (box: one stage of codes x 128 rows)
+  __half* hout;                // gate/up: H [rows][Fmax] fp16 (column-permuted for int4)
   float* yout;                 // down: Y [rows][d] fp32
 };
+
+constexpr int kPfACol = 256;        // first TMEM column of the A ring
+constexpr int kPfAStageCols = 64;   // 128 x 128 fp16 per stage
 
 template <int QT, bool GU>
 struct PfLayout {
   static constexpr int kMats = GU ? 2 : 1;
-  static constexpr int kRawRow = QT == COLI_Q_INT4_G128 ? 32 : 64;   // bytes of 64 codes
-  static constexpr int kRawBytes = kPfM * kRawRow;
-  static constexpr int kStageBytes = kMats * (kPfABytes + kRawBytes) + kPfBBytes;
-  static constexpr int kStages = (220 * 1024) / kStageBytes;
-  // stage: [A_0][A_1][B][raw_0][raw_1]  (A, B 1024-aligned)
-  static constexpr int kOffB = kMats * kPfABytes;
-  static constexpr int kOffRaw = kOffB + kPfBBytes;
-  static constexpr int kTmemCols = GU ? 512 : 256;
+  static constexpr int kStageK = prefill_stage_k(GU);            // K per stage (64 or 128)
+  static constexpr int kAtoms = kStageK / 64;                    // 128-byte activation atoms per stage
+  static constexpr int kRawRow = prefill_raw_row_bytes(QT, GU);  // bytes of one row's codes per stage
+  static constexpr int kRawBytes = kPfM * kRawRow;               // per matrix
+  static constexpr int kBAtomBytes = kPfN * 128;                 // 128 token rows x 64 fp16
+  static constexpr int kBBytes = kAtoms * kBAtomBytes;
+  static constexpr int kStageBytes = kBBytes + kMats * kRawBytes;
+  static constexpr int kStagesFit = (216 * 1024) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kSmemBytes = kStages * kStageBytes;
+  static constexpr int kAccSets = GU ? 1 : 2;                    // TMEM columns 0..255 hold the accumulators
+  static constexpr int kCodesPerThread = 32;                     // per dequantising thread and stage
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+  static_assert(kRawRow == 32 || kRawRow == 64 || kRawRow == 128, "raw box width");
+  static_assert(kPfAStages * kPfAStageCols + kPfACol <= 512, "TMEM budget");
 };
 
 template <int QT, bool GU>
@@ -234,7 +313,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   constexpr bool I4 = QT == COLI_Q_INT4_G128;
   constexpr int S = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ uint64_t full_tma[S], full_a[S], empty[S], acc_full, acc_empty;
+  __shared__ uint64_t tma_full[S], tma_empty[S], a_full[kPfAStages], a_empty[kPfAStages], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -244,18 +323,23 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full_tma[s], 1);
-      mbar_init(&full_a[s], kPfDqWarps);
-      mbar_init(&empty[s], 1);
+      mbar_init(&tma_full[s], 1);
+      mbar_init(&tma_empty[s], 1);
     }
-    mbar_init(&acc_full, 1);
-    mbar_init(&acc_empty, kPfDqWarps);
+    for (int s = 0; s < kPfAStages; ++s) {
+      mbar_init(&a_full[s], kPfDqWarps);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_empty[s], kPfEpWarps);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "r"(L::kTmemCols));
+                 "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -280,28 +364,51 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
+      // raw weight codes come from HBM: an L2 prefetch runs kPfPrefetch stages ahead of the
+      // loads (also across tile boundaries) so that the loads into shared memory hit L2
+      constexpr int kPfPrefetch = 8;
+      int pf_t = blockIdx.x, pf_kb = 0, pf_nkb = 0, pf_slot = 0, pf_mb = 0;
+      auto pf_load = [&]() {
+        if (pf_t < n_tiles) {
+          int r0, nt, K;
+          tile_info(pf_t, pf_slot, r0, nt, pf_mb, K);
+          pf_nkb = K / L::kStageK;
+        }
+      };
+      auto pf_step = [&]() {
+        if (pf_t >= n_tiles) return;
+        for (int m = 0; m < L::kMats; ++m)
+          tma_prefetch_2d(p.wmaps + (size_t)pf_slot * 3 + (GU ? m : 2), pf_kb * L::kRawRow, pf_mb * kPfM);
+        if (++pf_kb == pf_nkb) { pf_kb = 0; pf_t += gridDim.x; pf_load(); }
+      };
+      pf_load();
+      for (int j = 0; j < kPfPrefetch; ++j) pf_step();
       int it = 0;
       for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x) {
         int slot, row0, ntok, mb, K;
         tile_info(t, slot, row0, ntok, mb, K);
-        const int nkb = K / kPfKB, nbox = (ntok + kPfBBox - 1) / kPfBBox;
-        const uint32_t tx = (uint32_t)(L::kMats * L::kRawBytes + nbox * kPfBBox * 128);
+        const int nkb = K / L::kStageK, nbox = (ntok + kPfBBox - 1) / kPfBBox;
+        const uint32_t tx = (uint32_t)(L::kMats * L::kRawBytes + L::kAtoms * nbox * kPfBBox * 128);
+        bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
+          pf_step();
           const int s = it % S;
-          if (it >= S && !mbar_wait(&empty[s], ((it / S) - 1) & 1)) { fail_wait(); break; }
+          if (it >= S && !mbar_wait(&tma_empty[s], ((it / S) - 1) & 1)) { ok = false; break; }
           uint8_t* st = smem + (size_t)s * L::kStageBytes;
-          mbar_arrive_expect_tx(&full_tma[s], tx);
+          mbar_arrive_expect_tx(&tma_full[s], tx);
           for (int m = 0; m < L::kMats; ++m)
-            tma_load_2d_nohint(st + L::kOffRaw + m * L::kRawBytes, p.wmaps + (size_t)slot * 3 + (GU ? m : 2),
-                               kb * L::kRawRow, mb * kPfM, &full_tma[s]);
-          for (int b = 0; b < nbox; ++b)
-            tma_load_2d_nohint(st + L::kOffB + b * kPfBBox * 128, &bmap, kb * kPfKB, row0 + b * kPfBBox,
-                               &full_tma[s]);
+            tma_load_2d_nohint(st + L::kBBytes + m * L::kRawBytes, p.wmaps + (size_t)slot * 3 + (GU ? m : 2),
+                               kb * L::kRawRow, mb * kPfM, &tma_full[s]);
+          for (int at = 0; at < L::kAtoms; ++at)
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_nohint(st + at * L::kBAtomBytes + b * kPfBBox * 128, &bmap, kb * L::kStageK + at * 64,
+                                 row0 + b * kPfBBox, &tma_full[s]);
         }
+        if (!ok) { fail_wait(); break; }
       }
       // drain: every issued stage must have landed before the CTA can exit
       const int issued = it;
-      for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&full_tma[j % S], (j / S) & 1);
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_full[j % S], (j / S) & 1);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
@@ -310,158 +417,168 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x, ++tcount) {
         int slot, row0, ntok, mb, K;
         tile_info(t, slot, row0, ntok, mb, K);
-        const int nkb = K / kPfKB;
+        const int nkb = K / L::kStageK;
         const int N = (ntok + 15) & ~15;
         const uint32_t idesc = umma_idesc_f16(kPfM, N);
-        if (tcount > 0) {
-          if (!mbar_wait(&acc_empty, (tcount - 1) & 1)) { fail_wait(); break; }
+        const int acc = GU ? 0 : (tcount & 1);
+        const int uses = GU ? tcount : (tcount >> 1);   // earlier tiles that used this accumulator set
+        if (uses > 0) {
+          if (!mbar_wait_spin(&acc_empty[acc], (uses - 1) & 1)) { fail_wait(); break; }
           tc_fence_after();
         }
+        const uint32_t dacc = tmem + (uint32_t)(acc * 128);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % S;
-          if (!mbar_wait(&full_a[s], (it / S) & 1)) { ok = false; break; }
+          const int s = it % S, as = it % kPfAStages;
+          // a_full also covers the stage's TMA data: every dequantising warp waited for
+          // tma_full[s] (raw codes and activations share that barrier) before arriving
+          if (!mbar_wait_spin(&a_full[as], (it / kPfAStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + (size_t)s * L::kStageBytes);
-#pragma unroll
-          for (int k = 0; k < kPfKB / 16; ++k) {
-            const uint64_t bd = umma_desc_sw128(st + L::kOffB + k * 32);
-            for (int m = 0; m < L::kMats; ++m)
-              umma_f16(tmem + m * 256, umma_desc_sw128(st + m * kPfABytes + k * 32), bd, idesc,
-                       (kb > 0 || k > 0) ? 1u : 0u);
-          }
-          umma_commit(&empty[s]);
+          const uint32_t A = tmem + (uint32_t)(kPfACol + as * kPfAStageCols);
+          const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
+          if (GU) umma_stage_gu(dacc, A, bd, idesc, (uint32_t)kb);
+          else umma_stage_dn(dacc, A, bd, idesc, (uint32_t)kb, (uint32_t)(L::kBAtomBytes >> 4));
+          umma_commit(&tma_empty[s]);
+          umma_commit(&a_empty[as]);
         }
         if (!ok) { fail_wait(); break; }
-        umma_commit(&acc_full);
+        umma_commit(&acc_full[acc]);
       }
       // wait for the MMAs in flight before the CTA releases TMEM
-      if (it > 0) mbar_wait(&empty[(it - 1) % S], ((it - 1) / S) & 1);
+      if (it > 0) mbar_wait(&a_empty[(it - 1) % kPfAStages], ((it - 1) / kPfAStages) & 1);
     }
-  } else {
-    // ---------------------------------------------------------------- dequantise + epilogue (warps 2..9)
-    const int dt = threadIdx.x - 64;               // 0..255
-    const int r = dt & 127;                        // weight row within the tile
-    const int half = dt >> 7;                      // gate/up: matrix; down: which 32 codes
-    const int sp = warp & 3;                       // TMEM sub-partition of this warp
-    const int colhalf = (warp - 2) >> 2;           // epilogue: which half of the 16-column groups
-    int it = 0, tcount = 0;
+  } else if (warp < 2 + kPfEpWarps) {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int sp = warp & 3;                       // TMEM sub-partition: lanes 32*sp .. +31
+    int tcount = 0;
     for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x, ++tcount) {
       int slot, row0, ntok, mb, K;
       tile_info(t, slot, row0, ntok, mb, K);
-      const int nkb = K / kPfKB;
-      const DevExpert& ex = a.experts[slot];
-      const int mat = GU ? half : 2;
-      const DevMat& M = ex.m[mat];
-      const int wrow = mb * kPfM + r;
-      const int G = K / 128, ZB = (G + 1) / 2;
-      uint32_t zz8 = 0;
-      if (!I4) {
-        const uint32_t z = __ldg(M.z + wrow);
-        zz8 = (0x6400u | z) * 0x10001u;            // half2(1024 + z, 1024 + z)
-      }
-      bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % S;
-        uint32_t ss = 0, zz = zz8;
-        if (I4) {
-          const int g = (kb * kPfKB) / 128;
-          const uint16_t sb = __ldg(static_cast<const uint16_t*>(M.s) + (size_t)wrow * G + g);
-          const uint32_t zb = __ldg(M.z + (size_t)wrow * ZB + (g >> 1));
-          const uint32_t z = (zb >> ((g & 1) * 4)) & 15u;
-          ss = (uint32_t)sb * 0x10001u;
-          zz = (0x6400u | z) * 0x10001u;
-        }
-        if (!mbar_wait(&full_tma[s], (it / S) & 1)) { ok = false; break; }
-        uint8_t* st = smem + (size_t)s * L::kStageBytes;
-        uint8_t* A = st + (GU ? half * kPfABytes : 0);
-        const uint8_t* raw = st + L::kOffRaw + (GU ? half * L::kRawBytes : 0) + r * L::kRawRow;
-        // output 16-byte chunks c (8 fp16 each) of row r; down: this thread does 4 of the 8
-        const int c0 = GU ? 0 : half * 4, nc = GU ? 8 : 4;
-        for (int c = c0; c < c0 + nc; c += 4) {
-          uint4 out[4];
-          if (I4) {
-            const uint4 q = *reinterpret_cast<const uint4*>(raw + c * 4);   // 32 codes
-            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t h[4];
-              int4_word_to_h1024(qw[j], h);
-              out[j].x = h2_mul(h2_sub(h[0], zz), ss);
-              out[j].y = h2_mul(h2_sub(h[1], zz), ss);
-              out[j].z = h2_mul(h2_sub(h[2], zz), ss);
-              out[j].w = h2_mul(h2_sub(h[3], zz), ss);
-            }
-          } else {
-            const uint4* q4 = reinterpret_cast<const uint4*>(raw + c * 8);  // 32 codes
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const uint4 q = q4[j];
-              const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                uint32_t* o = reinterpret_cast<uint32_t*>(&out[2 * j + i]);
-                o[0] = h2_sub(__byte_perm(qw[2 * i], 0x64646464u, 0x4140), zz);
-                o[1] = h2_sub(__byte_perm(qw[2 * i], 0x64646464u, 0x4342), zz);
-                o[2] = h2_sub(__byte_perm(qw[2 * i + 1], 0x64646464u, 0x4140), zz);
-                o[3] = h2_sub(__byte_perm(qw[2 * i + 1], 0x64646464u, 0x4342), zz);
-              }
-            }
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<uint4*>(A + r * 128 + (((c + j) ^ (r & 7)) << 4)) = out[j];
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&full_a[s]);
-      }
-      if (!ok) { fail_wait(); break; }
-      // ---- epilogue: wait for the tile's accumulators
-      if (!mbar_wait(&acc_full, tcount & 1)) { fail_wait(); break; }
+      const int acc = GU ? 0 : (tcount & 1);
+      const int uses = GU ? tcount : (tcount >> 1);
+      if (!mbar_wait(&acc_full[acc], uses & 1)) { fail_wait(); break; }
       tc_fence_after();
-      const int trow = sp * 32 + lane;             // TMEM lane = weight row of this thread
-      const int orow = mb * kPfM + trow;
-      const uint32_t lane_addr = tmem + ((uint32_t)(sp * 32) << 16);
+      const DevExpert& ex = a.experts[slot];
+      const int orow = mb * kPfM + sp * 32 + lane;  // weight row of this thread (TMEM lane)
+      const uint32_t lane_addr = tmem + ((uint32_t)(sp * 32) << 16) + (uint32_t)(acc * 128);
       float s0 = 1.f, s1 = 1.f;
       if (!I4) {
         s0 = __ldg(static_cast<const float*>(ex.m[GU ? 0 : 2].s) + orow);
         if (GU) s1 = __ldg(static_cast<const float*>(ex.m[1].s) + orow);
       }
+      // column of H that holds hidden unit orow (see the file header)
+      const int hcol = I4 ? ((orow & ~7) | ((orow & 3) << 1) | ((orow >> 2) & 1)) : orow;
       const int ngroups = (ntok + 15) / 16;
-      for (int g16 = colhalf; g16 < ngroups; g16 += 2) {
-        float v0[16];
-        tmem_ld16(lane_addr + g16 * 16, v0);
+      for (int g16 = 0; g16 < ngroups; ++g16) {
+        uint32_t r0[16];
+        tmem_ld16_issue(lane_addr + g16 * 16, r0);
         if (GU) {
-          float v1[16];
-          tmem_ld16(lane_addr + 256 + g16 * 16, v1);
+          uint32_t r1[16];
+          tmem_ld16_issue(lane_addr + 128 + g16 * 16, r1);
+          tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int tcol = g16 * 16 + i;
             if (tcol < ntok) {
-              const float gv = v0[i] * s0, uv = v1[i] * s1;
+              const float gv = __uint_as_float(r0[i]) * s0, uv = __uint_as_float(r1[i]) * s1;
               const float hv = gv / (1.0f + expf(-gv)) * uv;
-              p.hout[(size_t)(row0 + tcol) * a.Fmax + orow] = __float2half_rn(hv);
+              p.hout[(size_t)(row0 + tcol) * a.Fmax + hcol] = __float2half_rn(hv);
             }
           }
         } else {
+          tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int tcol = g16 * 16 + i;
-            if (tcol < ntok) p.yout[(size_t)(row0 + tcol) * a.d + orow] = v0[i] * s0;
+            if (tcol < ntok) p.yout[(size_t)(row0 + tcol) * a.d + orow] = __uint_as_float(r0[i]) * s0;
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty);
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+    }
+  } else {
+    // ---------------------------------------------------------------- dequantise (warps 6..21)
+    // thread = (TMEM lane = weight row r, part g): 32 codes of row r per stage.
+    // gate/up: g -> (matrix g & 1, K half g >> 1); down: g -> K quarter.
+    const int sp = warp & 3, r = sp * 32 + lane;
+    const int g = (warp - 2 - kPfEpWarps) >> 2;      // 0..3
+    const int mat_i = GU ? (g & 1) : 0;
+    const int kpart = GU ? (g >> 1) : g;
+    const uint32_t tcol = (uint32_t)(GU ? mat_i * 32 + kpart * 16 : kpart * 16);
+    const uint32_t tlane = (uint32_t)(sp * 32) << 16;
+    int it = 0;
+    for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x) {
+      int slot, row0, ntok, mb, K;
+      tile_info(t, slot, row0, ntok, mb, K);
+      const int nkb = K / L::kStageK;
+      const DevMat& M = a.experts[slot].m[GU ? mat_i : 2];
+      const int wrow = mb * kPfM + r;
+      const int G = K / 128, ZB = (G + 1) / 2;
+      uint32_t zz8 = 0;
+      if (!I4) zz8 = (0x6400u | (uint32_t)__ldg(M.z + wrow)) * 0x10001u;   // half2(1024 + z)
+      // scale / zero-point of the stage's group (int4), fetched one stage ahead
+      auto load_sz = [&](int kb, uint32_t& sraw, uint32_t& zraw) {
+        const int grp = (kb * L::kStageK + kpart * 32) / 128;
+        sraw = __ldg(static_cast<const uint16_t*>(M.s) + (size_t)wrow * G + grp);
+        zraw = (__ldg(M.z + (size_t)wrow * ZB + (grp >> 1)) >> ((grp & 1) * 4)) & 15u;
+      };
+      uint32_t s_next = 0, z_next = 0;
+      if (I4) load_sz(0, s_next, z_next);
+      bool ok = true;
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const int s = it % S, as = it % kPfAStages;
+        uint32_t ss = 0, zz = zz8;
+        if (I4) {
+          ss = s_next * 0x10001u;
+          zz = (0x6400u | z_next) * 0x10001u;
+          if (kb + 1 < nkb) load_sz(kb + 1, s_next, z_next);
+        }
+        if (!mbar_wait(&tma_full[s], (it / S) & 1)) { ok = false; break; }
+        if (it >= kPfAStages) {
+          if (!mbar_wait(&a_empty[as], ((it / kPfAStages) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
+        const uint8_t* raw = smem + (size_t)s * L::kStageBytes + L::kBBytes + (GU ? mat_i * L::kRawBytes : 0) +
+                             r * L::kRawRow;
+        uint32_t o[16];
+        if (I4) {
+          const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, kpart) << 4)));
+          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            o[4 * j + 0] = h2_mul(h2_sub(nib2_h1024(qw[j]), zz), ss);
+            o[4 * j + 1] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 4), zz), ss);
+            o[4 * j + 2] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 8), zz), ss);
+            o[4 * j + 3] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 12), zz), ss);
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, 2 * kpart + h) << 4)));
+            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              o[8 * h + 2 * j] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4140), zz);
+              o[8 * h + 2 * j + 1] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4342), zz);
+            }
+          }
+        }
+        tmem_st16(tmem + tlane + (uint32_t)(kPfACol + as * kPfAStageCols) + tcol, o);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[as]);
+      }
+      if (!ok) { fail_wait(); break; }
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
 }
 
@@ -471,7 +588,8 @@ template <int QT, bool GU>
 static cudaError_t launch_pf(const FwdArgs& a, const PfArgs& p, const CUtensorMap& bmap, cudaStream_t st,
                              int num_sms) {
   using L = PfLayout<QT, GU>;
-  const size_t smem = (size_t)L::kStages * L::kStageBytes + 1024;
+  const size_t smem = (size_t)L::kSmemBytes + 1024;
+  static_assert(L::kSmemBytes + 1024 <= 227 * 1024, "shared memory");
   auto kern = prefill_ffn_kernel<QT, GU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
