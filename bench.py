@@ -102,17 +102,17 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload
 
-def workload_setup(name: str):
+def workload_setup(name: str, experts: int = 0, tokens: int = 0):
+    """(workload, T of the JSON line, all T measured).  `experts` / `tokens` shrink the workload for
+    profiler captures (a few GB on the device); the default bench line uses the full configuration."""
+    import dataclasses
     w = H.WORKLOADS[name]
-    if name == "decode":
-        return w, 1, (1, 4)
-    if name == "mtp_verify":
-        return w, 3, (3,)
-    if name == "prefill":
-        return w, 2048, (2048,)
-    if name == "stacked":
-        return w, 256, (256,)
-    raise ValueError(name)
+    if experts:
+        w = dataclasses.replace(w, E=experts)
+    Ts = {"decode": (1, 4), "mtp_verify": (3,), "prefill": (2048,), "stacked": (256,)}[name]
+    if tokens:
+        Ts = (tokens,)
+    return w, Ts[0], Ts
 
 
 def unique_expert_bytes(dl, T) -> tuple[int, int]:
@@ -129,6 +129,20 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
     return gub, dnb
 
 
+# DRAM bytes per launch of the dominant decode kernel, from the ncu capture summarised in
+# profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
+# launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
+# that kernel changes, until it is captured again.
+DECODE_GATEUP_T1_TRAFFIC = 122_135_552 + 2_934_016
+
+
+def expert_flops(layer, T: int) -> tuple[float, float]:
+    """(gate/up FLOPs, down FLOPs) of one forward: every routed (token, expert) pair and every
+    shared-expert row, 2 FLOPs per multiply-add; padding of the MMA N dimension is not counted."""
+    pairs_f = T * layer.k * layer.F + (T * layer.F_shared if layer.shared is not None else 0)
+    return 2.0 * 2 * layer.d * pairs_f, 2.0 * layer.d * pairs_f
+
+
 def bench_native(args, rank: int, world: int):
     import torch
     import quantized_expert_ffn_bias_gb300 as coli
@@ -137,13 +151,16 @@ def bench_native(args, rank: int, world: int):
     coli.build()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    w, T_main, Ts = workload_setup(args.workload)
+    w, T_main, Ts = workload_setup(args.workload, args.experts, args.tokens)
     if args.workload == "stacked":
         raise SystemExit("stacked bench: use tests (per-layer parity); bench reports single layers")
     t0 = time.time()
     layer = w.layer(0)
     dl = DeviceLayer(layer, max(Ts), device=dev)
     gen_s = time.time() - t0
+    set_bytes = layer.experts.gate.nbytes + layer.experts.up.nbytes + layer.experts.down.nbytes
+    if layer.shared is not None:
+        set_bytes += layer.shared.gate.nbytes + layer.shared.up.nbytes + layer.shared.down.nbytes
     stream = torch.cuda.current_stream(dev)
     K, W = args.steps, args.warmup
     pk = peaks()
@@ -219,6 +236,29 @@ def bench_native(args, rank: int, world: int):
         achieved = (r["gub"] / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
         achieved_d = (r["dnb"] / dn_n) / (dn_ms / dn_n * 1e-3) / 1e9 if dn_n else None
         layer_gbs = (r["gub"] + r["dnb"]) / K / (ms_tot / K * 1e-3) / 1e9
+        if args.workload == "prefill":
+            # dense contraction: the tensor-core grouped GEMMs against the bf16/fp16 tensor peak
+            # (sustained figure: the kernels run inside multi-millisecond steps)
+            gfl, dfl = expert_flops(dl.layer, T)
+            tg_ms, tg_n = kt.get("tc_gate_up", (0.0, 0))
+            td_ms, td_n = kt.get("tc_down", (0.0, 0))
+            pk_t = pk["bf16_tflops_sustained"]
+            ach = gfl / (tg_ms / tg_n * 1e-3) / 1e12 if tg_n else None
+            ach_d = dfl / (td_ms / td_n * 1e-3) / 1e12 if td_n else None
+            layer_tf = (gfl + dfl) / (ms_tot / K * 1e-3) / 1e12
+            roof = {"bound": "tensor", "kernel": "tc_gate_up", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
+                    "frac": (ach / pk_t) if ach else None, "traffic": None,
+                    "peak_source": pk["source"] + " (bf16 dense, sustained; fp16 runs at the same rate)",
+                    "algorithmic_flops_per_launch": gfl, "down_kernel_achieved_tflops": ach_d,
+                    "layer_tflops": layer_tf, "layer_frac_of_burst_peak": layer_tf / pk["bf16_tflops"]}
+        else:
+            roof = {"bound": "hbm", "kernel": "expert_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                    "traffic": DECODE_GATEUP_T1_TRAFFIC if (T == 1 and args.workload == "decode"
+                                                            and not args.experts) else None,
+                    "peak_source": pk["source"],
+                    "algorithmic_bytes_per_launch": r["gub"] / max(gu_n, 1),
+                    "down_kernel_achieved_gbs": achieved_d}
         lines[T] = {
             "metric": METRIC,
             "value": world * K * T / (ms_tot * 1e-3),
@@ -226,11 +266,7 @@ def bench_native(args, rank: int, world: int):
             "ms_per_step": ms_tot / K,
             "hbm_gbs_layer": layer_gbs,
             "hbm_frac_layer": layer_gbs / pk["hbm_gbs"],
-            "roofline": {"bound": "hbm", "kernel": "expert_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
-                         "traffic": None, "peak_source": pk["source"],
-                         "algorithmic_bytes_per_launch": r["gub"] / max(gu_n, 1),
-                         "down_kernel_achieved_gbs": achieved_d},
+            "roofline": roof,
             "kernel_ms_per_step": {k: v[0] / v[1] for k, v in kt.items()},
             "kernel_share": {k: v[0] / max(sum(x[0] for x in kt.values()), 1e-12) for k, v in kt.items()},
             "kernel_sum_ms_per_step": step_kernel_ms,
@@ -239,7 +275,7 @@ def bench_native(args, rank: int, world: int):
             "gpu_launches": K * r["launches"],
             "clocks": r["clocks"],
         }
-    return w, T_main, Ts, lines, gen_s
+    return w, T_main, Ts, lines, gen_s, set_bytes
 
 
 def cpu_baseline(w, T: int, budget_s: float = 12.0):
@@ -272,6 +308,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode", choices=["decode", "mtp_verify", "prefill", "stacked"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=0, help="override E (reduced case for profiler captures)")
+    ap.add_argument("--tokens", type=int, default=0, help="override T (reduced case for profiler captures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -280,7 +318,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        w, T_main, Ts = workload_setup(args.workload)
+        w, T_main, Ts = workload_setup(args.workload, args.experts, args.tokens)
         import oracle as O
         layer = w.layer(0)
         orc = O.Oracle(layer)
@@ -312,7 +350,7 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    w, T_main, Ts, lines, gen_s = bench_native(args, rank, world)
+    w, T_main, Ts, lines, gen_s, set_bytes = bench_native(args, rank, world)
     if rank != 0:
         return
     line = dict(lines[T_main])
@@ -327,7 +365,8 @@ def main():
                    "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho,
                    "qtype": "int4-g128" if w.qtypes[0] == 0 else "int8-pc",
                    "shared_expert_d_ff": w.F_shared, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: 5.9 GB expert set, fresh x (fresh routing) every step",
+                   "l2": "inputs larger than L2: expert set of %.2f GB, fresh x (fresh routing) every step"
+                         % (set_bytes / 1e9),
                    "host_generation_s": round(gen_s, 1)},
         "cpu_baseline": cpu,
     })
