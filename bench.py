@@ -136,6 +136,23 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
 DECODE_GATEUP_T1_TRAFFIC = 122_135_552 + 2_934_016
 
 
+def max_over_ranks(v: float, device=None) -> float:
+    """Largest value over the ranks of the default process group (the time every replica must wait for);
+    identity without one.  Replicas exchange nothing else: the layer runs independently on every GPU."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tokens_per_s(world: int, steps: int, T: int, ms_max: float) -> float:
+    """Whole-job throughput: tokens all replicas processed / the slowest replica's time."""
+    return world * steps * T / (ms_max * 1e-3)
+
+
 def expert_flops(layer, T: int) -> tuple[float, float]:
     """(gate/up FLOPs, down FLOPs) of one forward: every routed (token, expert) pair and every
     shared-expert row, 2 FLOPs per multiply-add; padding of the MMA N dimension is not counted."""
@@ -184,6 +201,8 @@ def bench_native(args, rank: int, world: int):
                 dl.forward(xs[W + i], out=out)
             e1.record(stream)
             torch.cuda.synchronize(dev)
+            if world > 1:
+                torch.distributed.barrier()
         ms = e0.elapsed_time(e1)
         launches = dl.plan.last_launch_count()
         # ---- per-kernel times (same steps again, kernel-boundary events recorded by the library)
@@ -217,13 +236,8 @@ def bench_native(args, rank: int, world: int):
         results[T] = dict(ms=ms, kt=kt, launches=launches, gub=gub, dnb=dnb, clocks=clk.summary(), e2e_s=e2e_s,
                           h2d=xh[0].numel() * xh[0].element_size(), d2h=T * layer.d * 4)
         del xs
-    # reduce over ranks: max time
     def mx(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return max_over_ranks(v, dev)
 
     lines = {}
     for T, r in results.items():
@@ -261,7 +275,7 @@ def bench_native(args, rank: int, world: int):
                     "down_kernel_achieved_gbs": achieved_d}
         lines[T] = {
             "metric": METRIC,
-            "value": world * K * T / (ms_tot * 1e-3),
+            "value": replica_tokens_per_s(world, K, T, ms_tot),
             "unit": "tokens/s",
             "ms_per_step": ms_tot / K,
             "hbm_gbs_layer": layer_gbs,
