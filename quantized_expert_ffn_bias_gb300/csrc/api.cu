@@ -124,6 +124,8 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.logits = take((size_t)kRouterKSplit * T * E * 4);
   w.xs = take(T * (size_t)d.d * 4);
   w.xsum = take(T * (size_t)(d.d / kXsumBlock) * 4);
+  w.xq = take(T * (size_t)d.d * 2);
+  w.xqs = take(T * (size_t)(d.d / kXqBlock) * 8);
   w.h = take(rows * (size_t)p->Fmax * 4);
   w.hsum = take(rows * (size_t)(p->Fmax / 8) * 4);
   w.y = take(rows * (size_t)d.d * 4);
@@ -287,6 +289,8 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   a.logits = reinterpret_cast<float*>(ws + w.logits);
   a.xs = reinterpret_cast<float*>(ws + w.xs);
   a.xsum = reinterpret_cast<float*>(ws + w.xsum);
+  a.xq = reinterpret_cast<uint32_t*>(ws + w.xq);
+  a.xqs = reinterpret_cast<int2*>(ws + w.xqs);
   a.h = reinterpret_cast<float*>(ws + w.h);
   a.hsum = reinterpret_cast<float*>(ws + w.hsum);
   a.y = reinterpret_cast<float*>(ws + w.y);

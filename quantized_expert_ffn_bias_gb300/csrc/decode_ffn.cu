@@ -15,13 +15,24 @@
 // kDecodeStages-deep mbarrier pipeline; every wait is bounded and a timeout
 // sets the workspace status word.
 //
-// Exact dequantisation in fp32: a code c placed at mantissa bit 4p (int4) or
-// 8p (int8) of the float 2^23 gives 2^23 + c*16^p; subtracting 2^23 leaves
+// Per (row, group) the scale s and the zero point z enter once:
+// s*sum((c - z) x) = s*(sum(c x) - z*sum(x)).  The (s, z) pairs of the stage's
+// groups are built cooperatively in a 1 KB table per warp.
+//
+// int4 (integer dot products): the activations enter in 16-bit fixed point per
+// block of 32 inputs, x = sx*(256*hi + lo) with hi a signed and lo an unsigned
+// byte.  gate/up: prepared once per token by the routing kernel; down: each
+// lane converts its own 32 hidden values (one block) per stage.  Masking a word
+// of codes and its 4-bit shift with 0x0F0F0F0F gives the even and odd codes as
+// bytes, so one 8-code word costs three logic ops and four dp4a; sum(c*q) and
+// z*sum(q) are exact integers and one conversion per 32 codes brings them to
+// fp32.  The fixed point keeps every input to within 2^-16 of its block's
+// largest magnitude.
+//
+// int8 (exact fp32): a code c placed at mantissa bit 4p (int4)
+// or 8p (int8) of the float 2^23 gives 2^23 + c*16^p; subtracting 2^23 leaves
 // c*16^p exactly, and the activation was pre-multiplied by 16^-p (an exact
-// power of two), so the product is c*x.  Per (row, group) the scale s and the
-// zero-point z enter once: s*sum((c - z) x) = s*sum(c x) - (s*z)*sum(x); the
-// (s, s*z) pairs of the stage's groups are built cooperatively in a 1 KB table
-// and sum(x) is precomputed per block of inputs.
+// power of two), so the product is c*x; sum(x) is precomputed per block.
 #include "moe_internal.cuh"
 
 namespace coli {
@@ -231,6 +242,60 @@ __device__ __forceinline__ uint64_t dot_row_int8(uint4 w, const ulonglong2 (&x)[
 #undef COLI_WORD4
 #undef COLI_WORD8
 
+// One row slice of 32 int4 codes against the lane's fixed-point activations:
+// xh[8] / xl[8] = hi / lo bytes in unpack order.  Returns sum(c * q) exactly.
+__device__ __forceinline__ int dot_row_int4_dp4a(uint4 w, const uint32_t (&xh)[8], const uint32_t (&xl)[8]) {
+  int hi = 0;
+  uint32_t lo = 0;
+  const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t ev = q[j] & 0x0F0F0F0Fu, od = (q[j] >> 4) & 0x0F0F0F0Fu;
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hi) : "r"(ev), "r"(xh[2 * j]));
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(hi) : "r"(od), "r"(xh[2 * j + 1]));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(lo) : "r"(ev), "r"(xl[2 * j]));
+    asm("dp4a.u32.u32 %0, %1, %2, %0;" : "+r"(lo) : "r"(od), "r"(xl[2 * j + 1]));
+  }
+  return hi * 256 + (int)lo;
+}
+
+// 32 fp32 values (a lane's block) -> fixed point in the dot-product layout:
+// sx = 2^(floor(log2 max|v|) - 14), q = rint(v / sx) (|q| <= 32767).
+__device__ __forceinline__ void quantize32(const ulonglong2 (&v)[8], uint32_t (&xh)[8], uint32_t (&xl)[8], float& sx,
+                                           int& qsum) {
+  float f[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    f[4 * i] = __uint_as_float((uint32_t)v[i].x);
+    f[4 * i + 1] = __uint_as_float((uint32_t)(v[i].x >> 32));
+    f[4 * i + 2] = __uint_as_float((uint32_t)v[i].y);
+    f[4 * i + 3] = __uint_as_float((uint32_t)(v[i].y >> 32));
+  }
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(f[i]));
+  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+  e = e < -100 ? -100 : e;
+  sx = __uint_as_float((uint32_t)(e - 14 + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(14 - e + 127) << 23);
+  int q[32];
+  qsum = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    q[i] = min(__float2int_rn(f[i] * inv), 32767);
+    qsum += q[i];
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int od = 0; od < 2; ++od) {
+      const int* b = q + 8 * j + od;   // inputs 8j+od, +2, +4, +6
+      xh[2 * j + od] = __byte_perm(__byte_perm(b[0], b[2], 0x0051), __byte_perm(b[4], b[6], 0x0051), 0x5410);
+      xl[2 * j + od] = __byte_perm(__byte_perm(b[0], b[2], 0x0040), __byte_perm(b[4], b[6], 0x0040), 0x5410);
+    }
+  }
+}
+
 __device__ __forceinline__ float pair_sum(uint64_t p) {
   return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
 }
@@ -312,7 +377,9 @@ __device__ __forceinline__ ScaleRaw load_scales_int4(const DevExpert& ex, const 
   return o;
 }
 
-// Write the lane's four (s, s*z) entries of the stage table [16 rows][8 groups].
+// Write the lane's four entries of the stage table [16 rows][8 groups]:
+// (s, s*z) for the fp32 path, (s, z as int bits) for the integer path.
+template <bool DP>
 __device__ __forceinline__ void store_scales_int4(float2* tab, const ScaleRaw& o) {
   const int lane = threadIdx.x & 31;
   float2* dst = tab + (lane >> 1) * kGroupsPerStage + 4 * (lane & 1);
@@ -320,8 +387,8 @@ __device__ __forceinline__ void store_scales_int4(float2* tab, const ScaleRaw& o
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float s = f16_bits_to_float(sv[i]);
-    const float z = (float)((o.z4 >> (4 * i)) & 15u);
-    dst[i] = make_float2(s, s * z);
+    const int zi = (int)((o.z4 >> (4 * i)) & 15u);
+    dst[i] = DP ? make_float2(s, __int_as_float(zi)) : make_float2(s, s * (float)zi);
   }
 }
 
@@ -332,6 +399,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
                                          Cursor& prod, uint8_t* wbuf, uint64_t* bars, float2* tab, int& stage,
                                          uint32_t& phase, uint64_t policy) {
   constexpr bool I4 = QT == COLI_Q_INT4_G128;
+  constexpr bool DP = I4;               // integer dot products (fixed-point activations)
   constexpr int CODES = I4 ? 32 : 16;   // codes per lane per row per stage
   constexpr int XQ = CODES / 4;         // 16-byte activation loads per token
   const int lane = threadIdx.x & 31;
@@ -346,6 +414,8 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
   const int ntok = min(NT, u.cnt - cons.pass * kMaxNT);
   const float* xrow[NT];
   const float* srow[NT];
+  const uint32_t* qrow[NT];
+  const int2* qsrow[NT];
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const int tt = t < ntok ? t : 0;
@@ -356,6 +426,8 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       const int tok = a.pair_token[p0 + tt];
       xrow[t] = a.xs + (size_t)tok * a.d;
       srow[t] = a.xsum + (size_t)tok * (a.d / kXsumBlock);
+      qrow[t] = a.xq + (size_t)tok * (a.d / 2);
+      qsrow[t] = a.xqs + (size_t)tok * (a.d / kXqBlock);
     }
   }
   auto code0_of = [&](int kb) {
@@ -364,9 +436,19 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
   };
   auto load_x = [&](int t, int code0, ulonglong2 (&xq)[8], float& xsum) {
     const int c = code0 < 0 ? 0 : code0;
+    if constexpr (DP && !DOWN) {   // 64 bytes of hi/lo words (as 4 x 16 bytes) and the block's (sx, sum q)
+      const int b = c / kXqBlock;
+      const ulonglong2* src = reinterpret_cast<const ulonglong2*>(qrow[t] + (size_t)b * 16);
 #pragma unroll
-    for (int i = 0; i < XQ; ++i) xq[i] = ldg_nc_u64x2(xrow[t] + c + 4 * i);
-    if (DOWN) {          // sums of h over 8 consecutive inputs
+      for (int i = 0; i < 4; ++i) xq[i] = __ldg(src + i);
+      const int2 qs = __ldg(qsrow[t] + b);
+      xq[4].x = (unsigned long long)(uint32_t)qs.x | ((unsigned long long)(uint32_t)qs.y << 32);
+      return;
+    } else {
+#pragma unroll
+      for (int i = 0; i < XQ; ++i) xq[i] = ldg_nc_u64x2(xrow[t] + c + 4 * i);
+    if constexpr (DP) {  // int4 down: the block is converted where it is used
+    } else if (DOWN) {   // sums of h over 8 consecutive inputs
       if (I4) {
         const float4 h4 = __ldg(reinterpret_cast<const float4*>(srow[t] + c / 8));
         xsum = (h4.x + h4.y) + (h4.z + h4.w);
@@ -381,6 +463,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       } else {
         xsum = __ldg(srow[t] + c / kXsumBlock);
       }
+    }
     }
   };
 
@@ -413,9 +496,9 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
   bool ok = true;
   for (int kb = 0; kb < cons.n_kb; ++kb) {
     const int code0 = code0_of(kb);
-    if (I4) {                       // stage table of (s, s*z)
+    if (I4) {                       // stage table of (s, s*z) or (s, z)
       __syncwarp();
-      store_scales_int4(tab, sr);
+      store_scales_int4<DP>(tab, sr);
       __syncwarp();
     }
     // current-stage activations (token 0 prefetched); prefetch the next stage
@@ -434,12 +517,38 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         if (t > 0) load_x(t, code0, xq, xsum);
+        if (DP) {
+          uint32_t xh[8], xl[8];
+          float sx;
+          int qsum;
+          if constexpr (DOWN) {
+            quantize32(xq, xh, xl, sx, qsum);
+          } else {
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
-          const float2 sz = I4 ? tab[r * kGroupsPerStage + g] : tab[r];
-          const uint64_t d2 = I4 ? dot_row_int4(w, xq, m2) : dot_row_int8(w, xq, m2);
-          acc[t][r] = fmaf(sz.x, pair_sum(d2), fmaf(-sz.y, xsum, acc[t][r]));
+            for (int i = 0; i < 2; ++i) {
+              xh[4 * i] = (uint32_t)xq[i].x; xh[4 * i + 1] = (uint32_t)(xq[i].x >> 32);
+              xh[4 * i + 2] = (uint32_t)xq[i].y; xh[4 * i + 3] = (uint32_t)(xq[i].y >> 32);
+              xl[4 * i] = (uint32_t)xq[2 + i].x; xl[4 * i + 1] = (uint32_t)(xq[2 + i].x >> 32);
+              xl[4 * i + 2] = (uint32_t)xq[2 + i].y; xl[4 * i + 3] = (uint32_t)(xq[2 + i].y >> 32);
+            }
+            sx = __uint_as_float((uint32_t)xq[4].x);
+            qsum = (int)(uint32_t)(xq[4].x >> 32);
+          }
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
+            const float2 sz = tab[r * kGroupsPerStage + g];
+            const int comb = dot_row_int4_dp4a(w, xh, xl) - __float_as_int(sz.y) * qsum;
+            acc[t][r] = fmaf(sz.x * sx, (float)comb, acc[t][r]);
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
+            const float2 sz = I4 ? tab[r * kGroupsPerStage + g] : tab[r];
+            const uint64_t d2 = I4 ? dot_row_int4(w, xq, m2) : dot_row_int8(w, xq, m2);
+            acc[t][r] = fmaf(sz.x, pair_sum(d2), fmaf(-sz.y, xsum, acc[t][r]));
+          }
         }
       }
     }
@@ -466,13 +575,16 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       const float up = __shfl_down_sync(0xffffffffu, v, 16);
       const float hv = v / (1.0f + expf(-v)) * up;          // silu(gate) * up
       float hs = hv;                                           // sum of the 8 rows (lanes 0, 2, .., 14)
-      hs += __shfl_xor_sync(0xffffffffu, hs, 2);
-      hs += __shfl_xor_sync(0xffffffffu, hs, 4);
-      hs += __shfl_xor_sync(0xffffffffu, hs, 8);
+      if constexpr (!I4) {
+        hs += __shfl_xor_sync(0xffffffffu, hs, 2);
+        hs += __shfl_xor_sync(0xffffffffu, hs, 4);
+        hs += __shfl_xor_sync(0xffffffffu, hs, 8);
+      }
       const int row = u.rb * 8 + (lane >> 1);
+      // int4: plain h (the down kernel converts it to fixed point); int8: pre-scaled h and its sums
       if (lane < 16 && (lane & 1) == 0 && t < ntok)
-        a.h[(size_t)(p0 + t) * a.Fmax + row] = hv * act_prescale(QT, row);
-      if (lane == 0 && t < ntok) a.hsum[(size_t)(p0 + t) * (a.Fmax / 8) + u.rb] = hs;
+        a.h[(size_t)(p0 + t) * a.Fmax + row] = I4 ? hv : hv * act_prescale(QT, row);
+      if (!I4 && lane == 0 && t < ntok) a.hsum[(size_t)(p0 + t) * (a.Fmax / 8) + u.rb] = hs;
     }
   }
   return true;

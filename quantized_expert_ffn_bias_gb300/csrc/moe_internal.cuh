@@ -65,6 +65,8 @@ struct WsLayout {
   size_t logits;       // float [kRouterKSplit][T_max][E]
   size_t xs;           // float [T_max][d]  (dequant-GEMV input, pre-scaled)
   size_t xsum;         // float [T_max][d / kXsumBlock]  (unscaled block sums of x)
+  size_t xq;           // uint32 [T_max][d / 2]  16-bit fixed-point x as int8 hi / uint8 lo bytes (int4 decode)
+  size_t xqs;          // int2 [T_max][d / kXqBlock]  (block scale bits, sum of the fixed-point values)
   size_t h;            // float [P_max + T_max][Fmax]  (pre-scaled SwiGLU output)
   size_t hsum;         // float [P_max + T_max][Fmax / 8]  (unscaled sums of h over 8 rows)
   size_t y;            // float [P_max + T_max][d]
@@ -102,6 +104,8 @@ struct FwdArgs {
   float* logits;
   float* xs;
   float* xsum;
+  uint32_t* xq;
+  int2* xqs;                  // per block of kXqBlock inputs: (block scale bits, sum of the fixed-point values)
   float* h;
   float* hsum;
   float* y;
@@ -127,6 +131,13 @@ cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const vo
 cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
                                 const CUtensorMap* wmaps, const CUtensorMap& hmap, float* yout, cudaStream_t st,
                                 int num_sms);
+// int4 decode activations in 16-bit fixed point per block of kXqBlock inputs:
+// x ~= sx * q with sx a power of two (|q| < 2^15), q = 256 * hi + lo with hi a
+// signed and lo an unsigned byte.  Within a block, 64 bytes: 8 words of hi then
+// 8 words of lo; word 2w (2w+1) holds the bytes of inputs 8w+0,2,4,6 (8w+1,3,5,7),
+// the order in which the low (high) nibbles of a 32-bit word of codes unpack.
+constexpr int kXqBlock = 32;
+
 constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box height of the raw-code maps)
 constexpr int kPrefillChunk = 128;  // tokens per chunk (largest MMA N)
 
