@@ -120,6 +120,7 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.pair_slot = take(P * 4);
   w.pair_of = take(P * 4);
   w.unique = take((E + 1) * 4);
+  w.utab = take((E + 1) * 16);
   w.n_unique = take(16);
   w.logits = take((size_t)kRouterKSplit * T * E * 4);
   w.xs = take(T * (size_t)d.d * 4);
@@ -285,6 +286,7 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   a.pair_slot = reinterpret_cast<int32_t*>(ws + w.pair_slot);
   a.pair_of = reinterpret_cast<int32_t*>(ws + w.pair_of);
   a.unique = reinterpret_cast<int32_t*>(ws + w.unique);
+  a.utab = reinterpret_cast<int4*>(ws + w.utab);
   a.n_unique = reinterpret_cast<int32_t*>(ws + w.n_unique);
   a.logits = reinterpret_cast<float*>(ws + w.logits);
   a.xs = reinterpret_cast<float*>(ws + w.xs);

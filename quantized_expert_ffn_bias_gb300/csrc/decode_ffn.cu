@@ -62,21 +62,22 @@ __device__ __forceinline__ bool get_unit(const FwdArgs& a, int u, int n_routed, 
   const int rows = block_rows<DOWN>();
   const int per_routed = (DOWN ? a.d : a.F) / rows;
   const int routed_units = n_routed * per_routed;
-  int slot, rb;
+  int i, rb;
   if (u < routed_units) {
-    slot = a.unique[u / per_routed];
+    i = u / per_routed;
     rb = u % per_routed;
   } else {
     const int per_shared = (DOWN ? a.d : a.Fs) / rows;
     if (!a.has_shared || u - routed_units >= per_shared) return false;
-    slot = a.E;
+    i = n_routed;
     rb = u - routed_units;
   }
-  out.slot = slot;
+  const int4 e = __ldcg(a.utab + i);      // (slot, first pair row, pairs), written by the routing kernel
+  out.slot = e.x;
   out.rb = rb;
-  out.pbeg = a.offsets[slot];
-  out.cnt = a.offsets[slot + 1] - out.pbeg;
-  out.K = DOWN ? (slot == a.E ? a.Fs : a.F) : a.d;
+  out.pbeg = e.y;
+  out.cnt = e.z;
+  out.K = DOWN ? (e.x == a.E ? a.Fs : a.F) : a.d;
   return true;
 }
 

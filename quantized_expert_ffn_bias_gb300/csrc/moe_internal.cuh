@@ -61,6 +61,7 @@ struct WsLayout {
   size_t pair_slot;    // int32 [P_max]
   size_t pair_of;      // int32 [P_max]
   size_t unique;       // int32 [E+1]
+  size_t utab;         // int4 [E+1]: per entry of unique (+ shared): (slot, first pair row, pairs, 0); decode only
   size_t n_unique;     // int32 [4]
   size_t logits;       // float [kRouterKSplit][T_max][E]
   size_t xs;           // float [T_max][d]  (dequant-GEMV input, pre-scaled)
@@ -100,6 +101,7 @@ struct FwdArgs {
   int32_t* pair_slot;
   int32_t* pair_of;
   int32_t* unique;
+  int4* utab;
   int32_t* n_unique;
   float* logits;
   float* xs;

@@ -152,34 +152,61 @@ __device__ __forceinline__ void warp_argmax(float& u, int& e) {
   }
 }
 
-// Top-k of one token by one warp.  u, s: this warp's shared scratch [E] each.
-__device__ void topk_token(const FwdArgs& a, int t, float* u, float* s) {
+// Router scores of expert e for token t: s = sigmoid(z) with z the K-split
+// partial logits summed in split order, u = s + bias.
+__device__ __forceinline__ void router_scores(const FwdArgs& a, int t, int e, float& sv, float& uv) {
+  float z = 0.f;
+#pragma unroll
+  for (int ks = 0; ks < kRouterKSplit; ++ks) z += __ldcg(a.logits + ((size_t)ks * a.T + t) * a.E + e);
+  sv = 1.0f / (1.0f + expf(-z));
+  uv = sv + __ldg(a.bias + e);
+}
+
+// Best (score, expert) among a lane's NV scores (experts lane, lane + 32, ...);
+// ties -> lower expert id.
+template <int NV>
+__device__ __forceinline__ void lane_best(const float (&v)[NV], int lane, int nv, int E, float& bu, int& be) {
+  bu = -INFINITY;
+  be = 0x7fffffff;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    if (i < nv && e < E && better(v[i], e, bu, be)) { bu = v[i]; be = e; }
+  }
+}
+
+// Selection for one token by one warp from its scores in shared memory
+// (u, s: [E] each).  Writes topk_idx / topk_w / near_tie and,
+// if sel_out is given, the selected ids (ascending) to sel_out[0..k).
+// NV = scores per lane (8 keeps them in registers for E <= 256; 32 covers kMaxE).
+template <int NV>
+__device__ __forceinline__ void topk_select_nv(const FwdArgs& a, int t, float* u, const float* s, int* sel_out) {
   const int lane = threadIdx.x & 31;
   const int E = a.E, k = a.k;
-  for (int e = lane; e < E; e += 32) {
-    float z = 0.f;
+  // the lane's scores (experts lane, lane+32, ...) in registers; each round the
+  // warp takes the best lane candidate and only the winning lane rescans
+  const int nv = (E + 31) / 32;
+  float v[NV];
 #pragma unroll
-    for (int ks = 0; ks < kRouterKSplit; ++ks) z += __ldcg(a.logits + ((size_t)ks * a.T + t) * E + e);
-    const float sv = 1.0f / (1.0f + expf(-z));
-    s[e] = sv;
-    u[e] = sv + a.bias[e];
-  }
-  __syncwarp();
+  for (int i = 0; i < NV; ++i) v[i] = (i < nv && lane + 32 * i < E) ? u[lane + 32 * i] : -INFINITY;
+  float lbu;
+  int lbe;
+  lane_best(v, lane, nv, E, lbu, lbe);
   int my_sel = -1;          // lane j < k: the j-th pick (by u, descending)
   float kth = 0.f;
   for (int j = 0; j <= k && j < E; ++j) {
-    float bu = -INFINITY;
-    int be = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      const float v = u[e];
-      if (better(v, e, bu, be)) { bu = v; be = e; }
-    }
+    float bu = lbu;
+    int be = lbe;
     warp_argmax(bu, be);
     if (j < k) {
       if (lane == j) my_sel = be;
       kth = bu;
-      if (lane == 0) u[be] = -INFINITY;
-      __syncwarp();
+      if ((be & 31) == lane) {     // remove the pick from its lane and rescan that lane
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (i == (be >> 5)) v[i] = -INFINITY;
+        lane_best(v, lane, nv, E, lbu, lbe);
+      }
     } else {
       const float gap = kth - bu;
       if (lane == 0) a.near_tie[t] = gap < kNearTie ? 1 : 0;
@@ -204,8 +231,24 @@ __device__ void topk_token(const FwdArgs& a, int t, float* u, float* s) {
   if (lane < k) {
     a.topk_idx[(size_t)t * k + lane] = sorted_e;
     a.topk_w[(size_t)t * k + lane] = a.rho * my_s / ssum;
+    if (sel_out) sel_out[lane] = sorted_e;
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void topk_select(const FwdArgs& a, int t, float* u, const float* s, int* sel_out) {
+  static_assert(kMaxE == 32 * 32, "lane score array covers kMaxE");
+  if (a.E <= 256) topk_select_nv<8>(a, t, u, s, sel_out);
+  else topk_select_nv<32>(a, t, u, s, sel_out);
+}
+
+// Top-k of one token by one warp.  u, s: this warp's shared scratch [E] each.
+__device__ void topk_token(const FwdArgs& a, int t, float* u, float* s) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 8
+  for (int e = lane; e < a.E; e += 32) router_scores(a, t, e, s[e], u[e]);
+  __syncwarp();
+  topk_select(a, t, u, s, nullptr);
 }
 
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a) {
@@ -235,15 +278,37 @@ constexpr int kRouteThreads = 256;
 
 template <int NT, int XT>
 __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) {
-  extern __shared__ float sm[];            // last CTA: 8 warps x (u[E], s[E])
+  // dynamic shared memory (last CTA): per token (u[E], s[E])
+  extern __shared__ float sm[];
   __shared__ int is_last;
-  __shared__ int hist[kMaxE];
-  __shared__ int scan[kMaxE + 1];
+  __shared__ int hist[kDecodeMaxT * kMaxK];   // grouping: first pair of its expert
   __shared__ int sidx[kDecodeMaxT * kMaxK];
-  __shared__ int warp_tot[32];
-  __shared__ int total;
   const int tid = threadIdx.x, lane = tid & 31;
 
+  // (2) router GEMV partial logits.  The warp's first batch of weight loads is
+  //     issued before the activation conversion (1), which runs while they are
+  //     in flight; every lane of the warp takes part in (1).
+  //     CTA b covers K-split b % kRouterKSplit for experts 8*(b / kRouterKSplit) + warp.
+  constexpr int U = 16;
+  const int ks_r = blockIdx.x % kRouterKSplit;
+  const int e_w = (blockIdx.x / kRouterKSplit) * (kRouteThreads / 32) + (tid >> 5);
+  const bool has_row = e_w < a.E;
+  const int e_r = has_row ? e_w : 0;
+  const int L = a.d / kRouterKSplit, k0 = ks_r * L;
+  float* topk_sm = sm;
+  const float* wr = a.router_w + (size_t)e_r * a.d + k0;
+  float acc[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t] = 0.f;
+  float4 wv[U];
+  auto load_batch = [&](int base) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * 128;
+      wv[u] = (has_row && i < L) ? __ldg(reinterpret_cast<const float4*>(wr + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_batch(lane * 4);
   // (1) dequant-GEMV inputs, grid-stride: int4 -> 16-bit fixed point per block
   //     of kXqBlock inputs (one warp per block); int8 -> pre-scaled fp32 + block sums
   if (a.qtype == COLI_Q_INT4_G128) {
@@ -293,58 +358,43 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
       a.xsum[i] = sum;
     }
   }
-  // (2) router GEMV partial logits
-  {
-    const int gw = (blockIdx.x * kRouteThreads + tid) >> 5;
-    if (gw < a.E * kRouterKSplit) {
-      const int e = gw / kRouterKSplit, ks = gw % kRouterKSplit;
-      const int L = a.d / kRouterKSplit, k0 = ks * L;
-      const float* w = a.router_w + (size_t)e * a.d + k0;
-      float acc[NT];
+  for (int base = lane * 4; base < L; base += 128 * U) {
+    if (base != lane * 4) load_batch(base);
+    if (!has_row) continue;
 #pragma unroll
-      for (int t = 0; t < NT; ++t) acc[t] = 0.f;
-      constexpr int U = 16;
-      for (int base = lane * 4; base < L; base += 128 * U) {
-        float4 wv[U];
+    for (int t = 0; t < NT; ++t) {
+      if (t >= a.T) continue;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int i = base + u * 128;
-          wv[u] = i < L ? __ldg(reinterpret_cast<const float4*>(w + i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int u = 0; u < U; ++u) {
+        const int i = base + u * 128;
+        if (i >= L) continue;
+        float x0, x1, x2, x3;
+        if (XT == COLI_X_BF16) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) +
+                                                                (size_t)t * a.d + k0 + i));
+          x0 = __uint_as_float(xv.x << 16);
+          x1 = __uint_as_float(xv.x & 0xFFFF0000u);
+          x2 = __uint_as_float(xv.y << 16);
+          x3 = __uint_as_float(xv.y & 0xFFFF0000u);
+        } else {
+          const float4 xv =
+              __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * a.d + k0 + i));
+          x0 = xv.x; x1 = xv.y; x2 = xv.z; x3 = xv.w;
         }
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (t >= a.T) continue;
-#pragma unroll
-          for (int u = 0; u < U; ++u) {
-            const int i = base + u * 128;
-            if (i >= L) continue;
-            float x0, x1, x2, x3;
-            if (XT == COLI_X_BF16) {
-              const uint2 xv = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) +
-                                                                    (size_t)t * a.d + k0 + i));
-              x0 = __uint_as_float(xv.x << 16);
-              x1 = __uint_as_float(xv.x & 0xFFFF0000u);
-              x2 = __uint_as_float(xv.y << 16);
-              x3 = __uint_as_float(xv.y & 0xFFFF0000u);
-            } else {
-              const float4 xv =
-                  __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + (size_t)t * a.d + k0 + i));
-              x0 = xv.x; x1 = xv.y; x2 = xv.z; x3 = xv.w;
-            }
-            acc[t] = fmaf(x0, wv[u].x, acc[t]);
-            acc[t] = fmaf(x1, wv[u].y, acc[t]);
-            acc[t] = fmaf(x2, wv[u].z, acc[t]);
-            acc[t] = fmaf(x3, wv[u].w, acc[t]);
-          }
-        }
+        acc[t] = fmaf(x0, wv[u].x, acc[t]);
+        acc[t] = fmaf(x1, wv[u].y, acc[t]);
+        acc[t] = fmaf(x2, wv[u].z, acc[t]);
+        acc[t] = fmaf(x3, wv[u].w, acc[t]);
       }
+    }
+  }
+  if (has_row) {
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        float v = acc[t];
+    for (int t = 0; t < NT; ++t) {
+      float v = acc[t];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0 && t < a.T) a.logits[((size_t)ks * a.T + t) * a.E + e] = v;
-      }
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0 && t < a.T) a.logits[((size_t)ks_r * a.T + t) * a.E + e_r] = v;
     }
   }
   // (3) ticket: the last CTA to arrive does the rest
@@ -355,67 +405,79 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
   if (!is_last) return;
   __threadfence();
 
-  // (4) top-k, one warp per token
+  // (4) top-k: every thread loads scores (all loads independent), then one warp per token selects
+  for (int i = tid; i < a.T * a.E; i += kRouteThreads) {
+    const int t = i / a.E, e = i - t * a.E;
+    float* u = topk_sm + (size_t)t * 2 * a.E;
+    router_scores(a, t, e, u[a.E + e], u[e]);
+  }
+  __syncthreads();
   {
     const int warp = tid >> 5;
-    float* u = sm + (size_t)warp * 2 * a.E;
-    for (int t = warp; t < a.T; t += kRouteThreads / 32) topk_token(a, t, u, u + a.E);
+    for (int t = warp; t < a.T; t += kRouteThreads / 32) {
+      float* u = topk_sm + (size_t)t * 2 * a.E;
+      topk_select(a, t, u, u + a.E, sidx + t * a.k);
+    }
   }
   __syncthreads();
-  // (5) grouping of the P = T*k pairs (stable counting sort by expert id)
+  // (5) grouping of the P = T*k <= 256 pairs (stable counting sort by expert id),
+  //     by direct counting over the pairs: position of pair f = pairs with a lower
+  //     expert id, plus earlier pairs of the same expert
   const int E = a.E, P = a.T * a.k;
-  for (int e = tid; e < E; e += kRouteThreads) hist[e] = 0;
-  __syncthreads();
-  for (int f = tid; f < P; f += kRouteThreads) {
-    const int e = __ldcg(a.topk_idx + f);
-    sidx[f] = e;
-    if (e < 0 || e >= E) set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
-    else atomicAdd(&hist[e], 1);
-  }
-  __syncthreads();
-  int carry = 0;
-  for (int b = 0; b < E; b += kRouteThreads) {
-    const int e = b + tid;
-    const int ex = block_exclusive_scan(e < E ? hist[e] : 0, warp_tot, &total);
-    if (e < E) scan[e] = carry + ex;
-    carry += total;
-  }
-  if (tid == 0) scan[E] = carry;
-  __syncthreads();
   for (int f = tid; f < P; f += kRouteThreads) {
     const int e = sidx[f];
-    if (e < 0 || e >= E) continue;
-    int rank = 0;
-    for (int g = 0; g < f; ++g) rank += sidx[g] == e;
-    const int pos = scan[e] + rank;
+    if (e < 0 || e >= E) { set_status(a.status, COLI_DEV_BAD_EXPERT_ID); continue; }
+    int pos = 0, first = 1;
+    for (int g = 0; g < P; ++g) {
+      const int eg = sidx[g];
+      pos += (eg < e) || (eg == e && g < f);
+      first &= !(eg == e && g < f);
+    }
     a.pair_token[pos] = f / a.k;
     a.pair_slot[pos] = f % a.k;
     a.pair_of[f] = pos;
+    hist[f] = first;                 // first pair (in flat order) of its expert
   }
-  for (int e = tid; e <= E; e += kRouteThreads) a.offsets[e] = scan[e];
+  for (int e = tid; e <= E; e += kRouteThreads) {
+    int below = 0;
+    for (int g = 0; g < P; ++g) below += sidx[g] < e;
+    a.offsets[e] = below;
+  }
   if (tid == 0) a.offsets[E + 1] = P + (a.has_shared ? a.T : 0);
   if (a.has_shared)
     for (int t = tid; t < a.T; t += kRouteThreads) a.pair_token[P + t] = t;
-  int ucarry = 0;
-  for (int b = 0; b < E; b += kRouteThreads) {
-    const int e = b + tid;
-    const int fl = (e < E && hist[e] > 0) ? 1 : 0;
-    const int ex = block_exclusive_scan(fl, warp_tot, &total);
-    if (fl) a.unique[ucarry + ex] = e;
-    ucarry += total;
+  __syncthreads();
+  // experts with tokens, ascending: rank of each expert's first pair among the
+  // first pairs; utab gets (slot, first pair row, pairs) per entry for the
+  // dequant-GEMV kernels
+  for (int f = tid; f < P; f += kRouteThreads) {
+    if (!hist[f]) continue;
+    const int e = sidx[f];
+    int r = 0, below = 0, cnt = 0;
+    for (int g = 0; g < P; ++g) {
+      r += hist[g] && sidx[g] < e;
+      below += sidx[g] < e;
+      cnt += sidx[g] == e;
+    }
+    a.unique[r] = e;
+    a.utab[r] = make_int4(e, below, cnt, 0);
   }
   if (tid == 0) {
-    a.n_unique[0] = ucarry;
-    if (a.has_shared) a.unique[ucarry] = E;
+    int nu = 0;
+    for (int g = 0; g < P; ++g) nu += hist[g];
+    a.n_unique[0] = nu;
+    if (a.has_shared) {
+      a.unique[nu] = E;
+      a.utab[nu] = make_int4(E, P, a.T, 0);
+    }
     a.status[1] = 0;
   }
 }
 
 cudaError_t launch_route_decode(const FwdArgs& a, cudaStream_t st) {
-  const int warps = a.E * kRouterKSplit;
-  int blocks = (warps * 32 + kRouteThreads - 1) / kRouteThreads;
-  if (blocks < 1) blocks = 1;
-  const size_t smem = (size_t)(kRouteThreads / 32) * 2 * a.E * sizeof(float);
+  const int blocks = ((a.E + kRouteThreads / 32 - 1) / (kRouteThreads / 32)) * kRouterKSplit;
+  const size_t smem = (size_t)a.T * 2 * a.E * sizeof(float);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
 #define COLI_ROUTE(NT)                                                                                    \
   {                                                                                                       \
     auto kern = a.xtype == COLI_X_BF16 ? route_decode_kernel<NT, COLI_X_BF16> : route_decode_kernel<NT, COLI_X_F32>; \
