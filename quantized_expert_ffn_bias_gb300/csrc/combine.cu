@@ -9,6 +9,7 @@
 namespace coli {
 
 __global__ void combine_kernel(FwdArgs a) {
+  griddep_wait();                  // y of the expert kernels
   const int t = blockIdx.y;
   const int i4 = blockIdx.x * blockDim.x + threadIdx.x;  // float4 index within the row
   if (i4 * 4 >= a.d) return;
@@ -37,8 +38,8 @@ __global__ void combine_kernel(FwdArgs a) {
 cudaError_t launch_combine(const FwdArgs& a, cudaStream_t st) {
   const int threads = 256;
   dim3 grid((a.d / 4 + threads - 1) / threads, a.T);
-  combine_kernel<<<grid, threads, 0, st>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = launch_pdl(combine_kernel, grid, dim3(threads), 0, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ RMSNorm -> bf16

@@ -602,6 +602,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   uint64_t* bars = bars_all[warp];
   float2* tab = tabs[warp];
 
+  griddep_launch_dependents();
+  griddep_wait();                  // routing (gate/up) or h (down) of the previous kernel
   const int n_routed = a.n_unique[0];
   const int n_units = n_units_of<DOWN>(a, n_routed);
   const int stride = gridDim.x * kDecodeWarps;
@@ -651,8 +653,8 @@ static cudaError_t launch_decode_t(const FwdArgs& a, cudaStream_t st, int num_sm
   auto kern = decode_ffn_kernel<QT, DOWN, NTMAX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<num_sms, kDecodeWarps * 32, smem, st>>>(a);
-  return cudaGetLastError();
+  e = launch_pdl(kern, dim3(num_sms), dim3(kDecodeWarps * 32), smem, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <bool DOWN>

@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
   __shared__ int hist[kDecodeMaxT * kMaxK];   // grouping: first pair of its expert
   __shared__ int sidx[kDecodeMaxT * kMaxK];
   const int tid = threadIdx.x, lane = tid & 31;
+  griddep_launch_dependents();     // the expert kernel may start its prologue
 
   // (2) router GEMV partial logits.  The warp's first batch of weight loads is
   //     issued before the activation conversion (1), which runs while they are
