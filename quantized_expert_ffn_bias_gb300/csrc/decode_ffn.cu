@@ -487,12 +487,16 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
     for (int r = 0; r < kRows; ++r) acc[t][r] = 0.f;
 
   const uint64_t m2 = 0x4B0000004B000000ull;   // (2^23, 2^23)
-  // prefetch for stage 0: activations of the first token, scales
-  ulonglong2 xq0[8];
-  float xs0 = 0.f;
+  // activations of the first token and scales, loaded two stages ahead
+  ulonglong2 xq0[8], xq1[8];
+  float xs0 = 0.f, xs1 = 0.f;
+  ScaleRaw sr = {0u, 0u, 0u}, sr1 = {0u, 0u, 0u};
   load_x(0, code0_of(0), xq0, xs0);
-  ScaleRaw sr = {0u, 0u, 0u};
   if (I4) sr = load_scales_int4<DOWN>(ex, u, 0, G);
+  if (cons.n_kb > 1) {
+    load_x(0, code0_of(1), xq1, xs1);
+    if (I4) sr1 = load_scales_int4<DOWN>(ex, u, 1, G);
+  }
 
   bool ok = true;
   for (int kb = 0; kb < cons.n_kb; ++kb) {
@@ -502,14 +506,16 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       store_scales_int4<DP>(tab, sr);
       __syncwarp();
     }
-    // current-stage activations (token 0 prefetched); prefetch the next stage
+    // current-stage activations (token 0 prefetched); rotate and prefetch stage kb + 2
     ulonglong2 xq[8];
     float xsum = xs0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) xq[i] = xq0[i];
-    if (kb + 1 < cons.n_kb) {
-      load_x(0, code0_of(kb + 1), xq0, xs0);
-      if (I4) sr = load_scales_int4<DOWN>(ex, u, kb + 1, G);
+    for (int i = 0; i < 8; ++i) { xq[i] = xq0[i]; xq0[i] = xq1[i]; }
+    xs0 = xs1;
+    sr = sr1;
+    if (kb + 2 < cons.n_kb) {
+      load_x(0, code0_of(kb + 2), xq1, xs1);
+      if (I4) sr1 = load_scales_int4<DOWN>(ex, u, kb + 2, G);
     }
     const int g = I4 ? (code0 < 0 ? 0 : (code0 >> 7) - kb * kGroupsPerStage) : 0;
     if (!mbar_wait(bars + stage, phase)) { ok = false; break; }
