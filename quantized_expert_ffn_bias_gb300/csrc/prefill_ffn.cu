@@ -21,10 +21,10 @@
 // would be re-read by every MMA and shared-memory bandwidth would set the pace.
 //
 // int4 unpacking: a 32-bit word holds 8 codes n0..n7 (code i in bits 4i..4i+3).
-// Masking the word and its 4/8/12-bit shifts with 0x000F000F gives the pairs
-// (n0,n4), (n1,n5), (n2,n6), (n3,n7) in one logic op each, so within every
-// group of 8 inputs the A operand holds the codes in the order
-// 0,4,1,5,2,6,3,7.  The activation matrices (X for gate/up, H for down) are
+// Masking the word and its 8-bit shift with 0x000F000F (into fp16 1024 + c)
+// and with 0x00F000F0 (into fp16 64 + c) gives the pairs (n0,n4), (n1,n5),
+// (n2,n6), (n3,n7) with one shift and four logic ops, so within every group of
+// 8 inputs the A operand holds the codes in the order 0,4,1,5,2,6,3,7.  The activation matrices (X for gate/up, H for down) are
 // stored with the same permutation inside each group of 8 columns, which
 // leaves every dot product unchanged.  int8 keeps the natural order.
 //
@@ -262,8 +262,11 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
-// fp16 pair (1024 + (x & 15), 1024 + ((x >> 16) & 15)): exact, one logic op
-__device__ __forceinline__ uint32_t nib2_h1024(uint32_t x) { return (x & 0x000F000Fu) | 0x64006400u; }
+// fp16 pairs from the nibbles of a 32-bit word, exact, one logic op each:
+// bits 0-3 / 16-19 -> 1024 + c (exponent 10: mantissa unit 1),
+// bits 4-7 / 20-23 -> 64 + c   (exponent 6: mantissa bit 4 has weight 1).
+__device__ __forceinline__ uint32_t nib_lo_h1024(uint32_t x) { return (x & 0x000F000Fu) | 0x64006400u; }
+__device__ __forceinline__ uint32_t nib_hi_h64(uint32_t x) { return (x & 0x00F000F0u) | 0x54005400u; }
 
 // Physical 16-byte chunk of logical chunk c in row r of a TMA box with rows of
 // RB bytes stored with the RB-byte swizzle (RB = 32, 64 or 128).
@@ -518,22 +521,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int G = K / 128, ZB = (G + 1) / 2;
       uint32_t zz8 = 0;
       if (!I4) zz8 = (0x6400u | (uint32_t)__ldg(M.z + wrow)) * 0x10001u;   // half2(1024 + z)
-      // scale / zero-point of the stage's group (int4), fetched one stage ahead
+      // int4 scales / zero points: the row's 8-group batches (16 bytes of fp16 scales, 4 bytes
+      // of zero nibbles) are loaded a batch ahead when the layout allows vector loads,
+      // otherwise the stage's group is loaded one stage ahead
+      const uint16_t* srow = static_cast<const uint16_t*>(M.s) + (size_t)wrow * G;
+      const uint8_t* zrow = M.z + (size_t)wrow * ZB;
+      const bool vec = I4 && (G & 7) == 0 && ((reinterpret_cast<uintptr_t>(M.s) & 15) == 0) &&
+                       ((reinterpret_cast<uintptr_t>(M.z) & 3) == 0);
+      const int nbatch = G / 8;
+      uint4 sb = make_uint4(0, 0, 0, 0), sbn = sb;
+      uint32_t zb = 0, zbn = 0;
+      int cur_batch = 0;
+      auto load_batch = [&](int b, uint4& sv, uint32_t& zv) {
+        sv = __ldg(reinterpret_cast<const uint4*>(srow) + b);
+        zv = __ldg(reinterpret_cast<const uint32_t*>(zrow) + b);
+      };
+      auto grp_of = [&](int kb) { return (kb * L::kStageK + kpart * 32) / 128; };
       auto load_sz = [&](int kb, uint32_t& sraw, uint32_t& zraw) {
-        const int grp = (kb * L::kStageK + kpart * 32) / 128;
-        sraw = __ldg(static_cast<const uint16_t*>(M.s) + (size_t)wrow * G + grp);
-        zraw = (__ldg(M.z + (size_t)wrow * ZB + (grp >> 1)) >> ((grp & 1) * 4)) & 15u;
+        const int grp = grp_of(kb);
+        sraw = __ldg(srow + grp);
+        zraw = (__ldg(zrow + (grp >> 1)) >> ((grp & 1) * 4)) & 15u;
       };
       uint32_t s_next = 0, z_next = 0;
-      if (I4) load_sz(0, s_next, z_next);
+      if (vec) {
+        load_batch(0, sb, zb);
+        if (nbatch > 1) load_batch(1, sbn, zbn);
+      } else if (I4) {
+        load_sz(0, s_next, z_next);
+      }
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const int s = it % S, as = it % kPfAStages;
-        uint32_t ss = 0, zz = zz8;
+        uint32_t ss = 0, zz = zz8, zzh = 0;
         if (I4) {
-          ss = s_next * 0x10001u;
-          zz = (0x6400u | z_next) * 0x10001u;
-          if (kb + 1 < nkb) load_sz(kb + 1, s_next, z_next);
+          uint32_t sraw, zraw;
+          if (vec) {
+            const int grp = grp_of(kb);
+            if ((grp >> 3) != cur_batch) {
+              ++cur_batch;
+              sb = sbn;
+              zb = zbn;
+              if (cur_batch + 1 < nbatch) load_batch(cur_batch + 1, sbn, zbn);
+            }
+            const int gi = grp & 7;
+            const uint32_t sw = gi < 2 ? sb.x : gi < 4 ? sb.y : gi < 6 ? sb.z : sb.w;
+            sraw = (sw >> ((gi & 1) * 16)) & 0xFFFFu;
+            zraw = (zb >> (gi * 4)) & 15u;
+          } else {
+            sraw = s_next;
+            zraw = z_next;
+            if (kb + 1 < nkb) load_sz(kb + 1, s_next, z_next);
+          }
+          ss = sraw * 0x10001u;
+          zz = (0x6400u | zraw) * 0x10001u;          // half2(1024 + z)
+          zzh = (0x5400u | (zraw << 4)) * 0x10001u;  // half2(64 + z)
         }
         if (!mbar_wait(&tma_full[s], (it / S) & 1)) { ok = false; break; }
         if (it >= kPfAStages) {
@@ -548,10 +589,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            o[4 * j + 0] = h2_mul(h2_sub(nib2_h1024(qw[j]), zz), ss);
-            o[4 * j + 1] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 4), zz), ss);
-            o[4 * j + 2] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 8), zz), ss);
-            o[4 * j + 3] = h2_mul(h2_sub(nib2_h1024(qw[j] >> 12), zz), ss);
+            const uint32_t q8 = qw[j] >> 8;
+            o[4 * j + 0] = h2_mul(h2_sub(nib_lo_h1024(qw[j]), zz), ss);
+            o[4 * j + 1] = h2_mul(h2_sub(nib_hi_h64(qw[j]), zzh), ss);
+            o[4 * j + 2] = h2_mul(h2_sub(nib_lo_h1024(q8), zz), ss);
+            o[4 * j + 3] = h2_mul(h2_sub(nib_hi_h64(q8), zzh), ss);
           }
         } else {
 #pragma unroll
