@@ -117,29 +117,27 @@ __global__ void __launch_bounds__(256) plan_tiles_kernel(FwdArgs a, PfChunk* chu
   if (tid == 0) s_nchunks = carry;
   __syncthreads();
   const int nch = s_nchunks;
-  // tiles: gate/up rows F (F_shared for the shared slot), down rows d
-  int gcarry = 0, dcarry = 0;
-  for (int b = 0; b < nch; b += 256) {
-    const int c = b + tid;
-    int gm = 0, dm = 0;
-    if (c < nch) {
-      const int slot = chunks[c].slot;
-      gm = (slot == a.E ? a.Fs : a.F) / kPfM;
-      dm = a.d / kPfM;
-    }
-    const int gex = block_exclusive_scan(gm, warp_tot, &total);
-    const int gtot = total;
-    const int dex = block_exclusive_scan(dm, warp_tot, &total);
-    const int dtot = total;
-    for (int m = 0; m < gm; ++m) gu_tiles[gcarry + gex + m] = PfTile{c, m, 0, 0};
-    for (int m = 0; m < dm; ++m) dn_tiles[dcarry + dex + m] = PfTile{c, m, 0, 0};
-    gcarry += gtot;
-    dcarry += dtot;
+  // tiles: every chunk has F / 128 gate/up tiles (F_shared / 128 for the shared
+  // expert's chunks, which come last) and d / 128 down tiles; chunk-major order,
+  // written by all threads at once
+  const int n_sh = a.has_shared ? (a.T + kPfN - 1) / kPfN : 0;   // shared chunks (the last n_sh)
+  const int n_rt = nch - n_sh;
+  const int gm = a.F / kPfM, gms = a.Fs / kPfM, dm = a.d / kPfM;
+  const int n_gu = n_rt * gm + n_sh * gms, n_dn = nch * dm;
+  for (int i = tid; i < n_gu; i += blockDim.x) {
+    int c, m;
+    if (i < n_rt * gm) { c = i / gm; m = i - c * gm; }
+    else { const int j = i - n_rt * gm; c = n_rt + j / gms; m = j - (j / gms) * gms; }
+    gu_tiles[i] = PfTile{c, m, 0, 0};
+  }
+  for (int i = tid; i < n_dn; i += blockDim.x) {
+    const int c = i / dm;
+    dn_tiles[i] = PfTile{c, i - c * dm, 0, 0};
   }
   if (tid == 0) {
     counts[0] = nch;
-    counts[1] = gcarry;
-    counts[2] = dcarry;
+    counts[1] = n_gu;
+    counts[2] = n_dn;
   }
 }
 

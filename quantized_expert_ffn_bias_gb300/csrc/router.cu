@@ -60,52 +60,105 @@ __global__ void __launch_bounds__(256) router_gemv_kernel(FwdArgs a) {
 }
 
 // ------------------------------------------------------------------ large-T tiled GEMM
-// C[t][e] over one K-split: 64x64 tile per CTA, 256 threads, 4x4 outputs each.
-constexpr int RB_M = 64, RB_N = 64, RB_K = 32;
+// C[t][e] over one K-split: a (16*RM tokens) x 64 (experts) tile per CTA, 256
+// threads with RM x 4 outputs each, K in steps of 32.  The next K step's x and
+// Wr values are loaded into registers while the current step is computed from
+// shared memory (double-buffered, k-major so that each thread reads its
+// outputs' operands as two vector loads; columns XOR-swizzled by the k row so
+// that the transposing stores are free of bank conflicts).  fp32 FMA in
+// ascending k within the split.
+constexpr int RB_N = 64, RB_K = 32;
 
-template <int XT>
+template <int XT, int RM>
 __global__ void __launch_bounds__(256) router_gemm_kernel(FwdArgs a) {
-  __shared__ float As[RB_K][RB_M + 4];
-  __shared__ float Bs[RB_K][RB_N + 4];
+  constexpr int RB_M = 16 * RM;
+  constexpr int NA = RM / 2;                 // 4-element x loads per thread per K step
+  __shared__ __align__(16) float As[2][RB_K][RB_M];
+  __shared__ __align__(16) float Bs[2][RB_K][RB_N];
   const int tid = threadIdx.x;
   const int e0 = blockIdx.x * RB_N, t0 = blockIdx.y * RB_M, ks = blockIdx.z;
   const int L = a.d / kRouterKSplit, kbeg = ks * L;
-  const int tx = tid & 15, ty = tid >> 4;  // 16 x 16 threads, 4x4 each
-  float acc[4][4] = {};
-  for (int kk = 0; kk < L; kk += RB_K) {
-    // load A (x) tile 64 x 32 and B (Wr) tile 64 x 32: 2048 elements each, 8 per thread
-    for (int i = tid; i < RB_M * RB_K; i += 256) {
-      const int r = i / RB_K, c = i % RB_K;
-      const int t = t0 + r, k = kbeg + kk + c;
-      float v = 0.f;
+  const int tx = tid & 15, ty = tid >> 4;   // outputs: tokens RM*ty.., experts 4*tx..+3
+  // global -> register mapping: A rows ra + 32 i (token), 4 k at ca; B row rb (expert), 8 k at cb
+  const int ra = tid >> 3, ca = (tid & 7) * 4, rb = tid >> 2, cb = (tid & 3) * 8;
+  const bool vb = e0 + rb < a.E;
+  const float* wrow = a.router_w + (size_t)(e0 + rb) * a.d + kbeg + cb;
+  float4 ar[NA], br0, br1;
+  auto load_regs = [&](int kk) {
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+      const int t = t0 + ra + 32 * i;
       if (t < a.T) {
-        if (XT == COLI_X_BF16)
-          v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[(size_t)t * a.d + k] << 16);
-        else
-          v = static_cast<const float*>(a.x)[(size_t)t * a.d + k];
+        const size_t off = (size_t)t * a.d + kbeg + ca + kk;
+        if (XT == COLI_X_BF16) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.x) + off));
+          ar[i] = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                              __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+        } else {
+          ar[i] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(a.x) + off));
+        }
+      } else {
+        ar[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      As[c][r] = v;
-      const int e = e0 + r;
-      Bs[c][r] = e < a.E ? a.router_w[(size_t)e * a.d + k] : 0.f;
     }
-    __syncthreads();
-#pragma unroll 8
+    if (vb) {
+      br0 = __ldg(reinterpret_cast<const float4*>(wrow + kk));
+      br1 = __ldg(reinterpret_cast<const float4*>(wrow + kk + 4));
+    } else {
+      br0 = br1 = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  // swizzles: A column ^ (k & 28), B column ^ (((k >> 3) & 3) << 3)
+  auto store_regs = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < NA; ++i) {
+      const int sa = (ra + 32 * i) ^ (ca & 28);
+      As[buf][ca + 0][sa] = ar[i].x;
+      As[buf][ca + 1][sa] = ar[i].y;
+      As[buf][ca + 2][sa] = ar[i].z;
+      As[buf][ca + 3][sa] = ar[i].w;
+    }
+    const int sbc = rb ^ (((cb >> 3) & 3) << 3);
+    Bs[buf][cb + 0][sbc] = br0.x; Bs[buf][cb + 1][sbc] = br0.y; Bs[buf][cb + 2][sbc] = br0.z;
+    Bs[buf][cb + 3][sbc] = br0.w; Bs[buf][cb + 4][sbc] = br1.x; Bs[buf][cb + 5][sbc] = br1.y;
+    Bs[buf][cb + 6][sbc] = br1.z; Bs[buf][cb + 7][sbc] = br1.w;
+  };
+  float acc[RM][4] = {};
+  load_regs(0);
+  store_regs(0);
+  __syncthreads();
+  int buf = 0;
+  for (int kk = 0; kk < L; kk += RB_K) {
+    const bool more = kk + RB_K < L;
+    if (more) load_regs(kk + RB_K);
+#pragma unroll
     for (int c = 0; c < RB_K; ++c) {
-      float av[4], bv[4];
+      float av[RM];
+      if constexpr (RM == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(&As[buf][c][(ty * 2) ^ (c & 28)]);
+        av[0] = v.x; av[1] = v.y;
+      } else {
+        const float4 v = *reinterpret_cast<const float4*>(&As[buf][c][(ty * 4) ^ (c & 28)]);
+        av[0] = v.x; av[1] = v.y; av[2] = v.z; av[3] = v.w;
+      }
+      const float4 bv = *reinterpret_cast<const float4*>(&Bs[buf][c][(tx * 4) ^ (((c >> 3) & 3) << 3)]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[c][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[c][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+      for (int i = 0; i < RM; ++i) {
+        acc[i][0] = fmaf(av[i], bv.x, acc[i][0]);
+        acc[i][1] = fmaf(av[i], bv.y, acc[i][1]);
+        acc[i][2] = fmaf(av[i], bv.z, acc[i][2]);
+        acc[i][3] = fmaf(av[i], bv.w, acc[i][3]);
+      }
     }
-    __syncthreads();
+    if (more) {
+      store_regs(buf ^ 1);
+      __syncthreads();
+      buf ^= 1;
+    }
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = t0 + ty * 4 + i;
+  for (int i = 0; i < RM; ++i) {
+    const int t = t0 + ty * RM + i;
     if (t >= a.T) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -128,9 +181,15 @@ cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st) {
     else { COLI_GEMV(8) }
 #undef COLI_GEMV
   } else {
-    dim3 grid((a.E + RB_N - 1) / RB_N, (a.T + RB_M - 1) / RB_M, kRouterKSplit);
-    if (a.xtype == COLI_X_BF16) router_gemm_kernel<COLI_X_BF16><<<grid, 256, 0, st>>>(a);
-    else router_gemm_kernel<COLI_X_F32><<<grid, 256, 0, st>>>(a);
+    if (a.T >= 512) {       // 64-token tiles: 4 x 4 outputs per thread
+      dim3 grid((a.E + RB_N - 1) / RB_N, (a.T + 63) / 64, kRouterKSplit);
+      if (a.xtype == COLI_X_BF16) router_gemm_kernel<COLI_X_BF16, 4><<<grid, 256, 0, st>>>(a);
+      else router_gemm_kernel<COLI_X_F32, 4><<<grid, 256, 0, st>>>(a);
+    } else {                // 32-token tiles: more CTAs for small T
+      dim3 grid((a.E + RB_N - 1) / RB_N, (a.T + 31) / 32, kRouterKSplit);
+      if (a.xtype == COLI_X_BF16) router_gemm_kernel<COLI_X_BF16, 2><<<grid, 256, 0, st>>>(a);
+      else router_gemm_kernel<COLI_X_F32, 2><<<grid, 256, 0, st>>>(a);
+    }
   }
   return cudaGetLastError();
 }
