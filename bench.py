@@ -169,8 +169,6 @@ def bench_native(args, rank: int, world: int):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w, T_main, Ts = workload_setup(args.workload, args.experts, args.tokens)
-    if args.workload == "stacked":
-        raise SystemExit("stacked bench: use tests (per-layer parity); bench reports single layers")
     t0 = time.time()
     layer = w.layer(0)
     dl = DeviceLayer(layer, max(Ts), device=dev)
@@ -292,6 +290,130 @@ def bench_native(args, rank: int, world: int):
     return w, T_main, Ts, lines, gen_s, set_bytes
 
 
+def bench_stacked(args, world: int):
+    """Six stacked layers h <- h + MoE(bf16(RMSNorm(h))) per step (T=256, alternating int4 / int8 experts,
+    51.4 GB resident); a step is the whole stack on a fresh input."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+
+    coli.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w, T, _ = workload_setup("stacked", args.experts, args.tokens)
+    t0 = time.time()
+    dls, expert_bytes = [], []
+    for l in range(w.n_layers):
+        layer = w.layer(l)
+        dl = DeviceLayer(layer, T, device=dev)
+        per_expert = (layer.experts.gate.nbytes + layer.experts.up.nbytes + layer.experts.down.nbytes) // layer.E
+        expert_bytes.append((per_expert, layer.qtype))
+        dl.experts.bank = None          # keep only the device copies
+        dl.layer = None
+        dls.append((dl, layer.E, layer.k))
+        del layer
+    gen_s = time.time() - t0
+    set_bytes = sum(b * e for (b, _), (_, e, _) in zip(expert_bytes, dls))
+    stream = torch.cuda.current_stream(dev)
+    eps = w.rmsnorm_eps
+    K, W = args.steps, args.warmup
+    xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(K + W)]
+    h = torch.empty((T, w.d), dtype=torch.float32, device=dev)
+    h2 = torch.empty_like(h)
+    n = torch.empty((T, w.d), dtype=torch.int16, device=dev)
+
+    def step(x):
+        nonlocal h, h2
+        h.copy_(x.view(torch.bfloat16).float())
+        for dl, _, _ in dls:
+            coli.colibri_moe_rmsnorm_bf16(h, T, w.d, eps, n, stream)
+            dl.forward(n, out=h2, residual=h)
+            h, h2 = h2, h
+        return h
+
+    for i in range(W):
+        step(xs[i])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    with ClockSampler(dev.index) as clk:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for i in range(K):
+            step(xs[W + i])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    # per-kernel times and unique-expert bytes per layer
+    for dl, _, _ in dls:
+        dl.plan.profile_begin(K)
+    uniq = [0] * len(dls)
+    for i in range(K):
+        x = xs[W + i]
+        h.copy_(x.view(torch.bfloat16).float())
+        for li, (dl, E, k) in enumerate(dls):
+            coli.colibri_moe_rmsnorm_bf16(h, T, w.d, eps, n, stream)
+            dl.forward(n, out=h2, residual=h)
+            idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+            dl.plan.debug_routing(dl.ws, T, idx, stream=stream)
+            uniq[li] += int(torch.unique(idx).numel())
+            h, h2 = h2, h
+    torch.cuda.synchronize(dev)
+    kt_all = {}
+    for dl, _, _ in dls:
+        for kname, (tms, n_l) in dl.plan.profile_end().items():
+            a = kt_all.setdefault(kname, [0.0, 0])
+            a[0] += tms
+            a[1] += n_l
+    alg_bytes = sum(uniq[li] * expert_bytes[li][0] for li in range(len(dls))) / K   # per step
+    gu_ms, gu_n = kt_all.get("tc_gate_up", (0.0, 0))
+    gu_bytes = sum(uniq[li] * expert_bytes[li][0] * 2 // 3 for li in range(len(dls))) / K
+    pk = peaks()
+    ach = (gu_bytes * K / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
+    step_gbs = alg_bytes / (ms / K * 1e-3) / 1e9
+    # end to end through the public API: x (bf16) from pinned host memory, h back to pinned host memory
+    xh = [torch.empty_like(xs[0], device="cpu").pin_memory() for _ in range(K)]
+    for i in range(K):
+        xh[i].copy_(xs[W + i].cpu())
+    oh = torch.empty((K, T, w.d), dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(xs[0])
+    torch.cuda.synchronize(dev)
+    te = time.perf_counter()
+    for i in range(K):
+        xd.copy_(xh[i], non_blocking=True)
+        out = step(xd)
+        oh[i].copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - te, dev)
+    line = {
+        "metric": METRIC, "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
+        "ms_per_step": ms / K, "hbm_gbs_layer": step_gbs, "hbm_frac_layer": step_gbs / pk["hbm_gbs"],
+        "roofline": {"bound": "hbm", "kernel": "tc_gate_up", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": (ach / pk["hbm_gbs"]) if ach else None, "traffic": None, "peak_source": pk["source"],
+                     "algorithmic_bytes_per_launch": gu_bytes / len(dls)},
+        "kernel_ms_per_step": {k2: v[0] / K for k2, v in kt_all.items()},
+        "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": xh[0].numel() * xh[0].element_size(), "d2h_bytes_per_step": T * w.d * 4},
+        "gpu_launches": K * sum(dl.plan.last_launch_count() + 1 for dl, _, _ in dls),
+        "clocks": clk.summary(),
+        "n_gpus": world, "steps": K, "warmup": W, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4/int8-weights, fp16 tensor-core operands, f32 accumulate",
+        "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
+        "config": {"workload": f"stacked: 6 GLM-5.2-class MoE layers (int4, int8 alternating) with RMSNorm and "
+                               f"residual, T={T} tokens per step",
+                   "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho, "layers": w.n_layers,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: expert set of %.1f GB, fresh x every step" % (set_bytes / 1e9),
+                   "host_generation_s": round(gen_s, 1)},
+        "cpu_baseline": None,
+    }
+    return line
+
+
 def cpu_baseline(w, T: int, budget_s: float = 12.0):
     """The oracle as it stands on this host's cores, on a bounded sample of the workload's tokens."""
     import oracle as O
@@ -364,6 +486,11 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
+    if args.workload == "stacked":
+        line = bench_stacked(args, world)
+        if rank == 0:
+            print(json.dumps(line))
+        return
     w, T_main, Ts, lines, gen_s, set_bytes = bench_native(args, rank, world)
     if rank != 0:
         return
