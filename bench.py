@@ -133,7 +133,7 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_135_552 + 2_934_016
+DECODE_GATEUP_T1_TRAFFIC = 122_086_912 + 2_788_352
 
 
 def max_over_ranks(v: float, device=None) -> float:
