@@ -145,10 +145,10 @@ constexpr int kXqBlock = 32;
 constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box height of the raw-code maps)
 constexpr int kPrefillChunk = 128;  // tokens per chunk (largest MMA N)
 
-// K extent of one pipeline stage of the tensor-core path: 64 for gate/up (two
-// matrices per stage), 128 for down, so that every stage dequantises 128 x 128
-// fp16 weights.  The raw-code TMA box of a matrix is one stage wide.
-__host__ __device__ constexpr int prefill_stage_k(bool gate_up) { return gate_up ? 64 : 128; }
+// K extent of one pipeline stage of the tensor-core path (128: one int4 group
+// per stage; gate/up stages carry both matrices).  The raw-code TMA box of a
+// matrix is one stage wide.
+__host__ __device__ constexpr int prefill_stage_k(bool gate_up) { return gate_up ? 128 : 128; }
 __host__ __device__ constexpr int prefill_raw_row_bytes(int qtype, bool gate_up) {
   return qtype == COLI_Q_INT4_G128 ? prefill_stage_k(gate_up) / 2 : prefill_stage_k(gate_up);
 }

@@ -43,7 +43,7 @@ constexpr int kPfBBox = 64;         // activation rows per TMA box
 constexpr int kPfEpWarps = 4;       // epilogue warps (one per TMEM sub-partition)
 constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-partition)
 constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps) * 32;
-constexpr int kPfAStages = 4;       // TMEM A ring depth
+constexpr int kPfAStagesMax = 4;    // deepest TMEM A ring (barrier arrays)
 
 struct PfChunk { int slot, row0, ntok, pad; };
 struct PfTile { int chunk, mb, pad0, pad1; };
@@ -164,14 +164,16 @@ __device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
 // is on the critical path of the tensor pipe, so it executes as few
 // instructions per MMA as possible.  `kb` is the stage's index within the
 // tile: stage 0 overwrites the accumulators, later stages add to them.
-// gate/up: A stage = [gate K64 | up K64] (32 columns each), B = one 128-byte atom.
-__device__ __forceinline__ void umma_stage_gu(uint32_t d_gate, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb) {
+// gate/up, four K16 steps of both matrices from one 128-byte B atom: gate A at
+// TMEM column a, up A at column a_up (each advancing 8 columns per step).
+__device__ __forceinline__ void umma_stage_gu(uint32_t d_gate, uint32_t a, uint32_t a_up, uint64_t b, uint32_t idesc,
+                                              uint32_t kb) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t.reg .b32 a0, a1, a2, a3, a4, a5, a6, a7, dup;\n\t.reg .b64 b1, b2, b3;\n\t"
       "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
       "add.u32 dup, %0, 128;\n\t"
-      "add.u32 a1, %1, 32;\n\tadd.u32 a2, %1, 8;\n\tadd.u32 a3, %1, 40;\n\t"
-      "add.u32 a4, %1, 16;\n\tadd.u32 a5, %1, 48;\n\tadd.u32 a6, %1, 24;\n\tadd.u32 a7, %1, 56;\n\t"
+      "mov.u32 a1, %5;\n\tadd.u32 a2, %1, 8;\n\tadd.u32 a3, %5, 8;\n\t"
+      "add.u32 a4, %1, 16;\n\tadd.u32 a5, %5, 16;\n\tadd.u32 a6, %1, 24;\n\tadd.u32 a7, %5, 24;\n\t"
       "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [dup], [a1], %2, %3, p;\n\t"
@@ -181,7 +183,7 @@ __device__ __forceinline__ void umma_stage_gu(uint32_t d_gate, uint32_t a, uint6
       "tcgen05.mma.cta_group::1.kind::f16 [dup], [a5], b2, %3, q;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %3, q;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [dup], [a7], b3, %3, q;\n\t}" ::"r"(d_gate),
-      "r"(a), "l"(b), "r"(idesc), "r"(kb));
+      "r"(a), "l"(b), "r"(idesc), "r"(kb), "r"(a_up));
 }
 // down: A stage = K128 (64 columns), B = two 128-byte atoms 16 * atom16 bytes apart.
 __device__ __forceinline__ void umma_stage_dn(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb,
@@ -284,8 +286,7 @@ struct PfArgs {
   float* yout;                 // down: Y [rows][d] fp32
 };
 
-constexpr int kPfACol = 256;        // first TMEM column of the A ring
-constexpr int kPfAStageCols = 64;   // 128 x 128 fp16 per stage
+constexpr int kPfACol = 256;        // first TMEM column of the A ring (columns 256..511)
 
 template <int QT, bool GU>
 struct PfLayout {
@@ -301,10 +302,14 @@ struct PfLayout {
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = kStages * kStageBytes;
   static constexpr int kAccSets = GU ? 1 : 2;                    // TMEM columns 0..255 hold the accumulators
+  static constexpr int kAStageCols = kMats * kStageK / 2;        // two fp16 per TMEM column
+  static constexpr int kAStages = 256 / kAStageCols;             // TMEM A ring depth
+  static constexpr int kParts = kMats * kStageK / 32 / 4;        // 32-code parts per dequantising thread
+  static_assert(kAStages <= kPfAStagesMax, "A ring");
   static constexpr int kCodesPerThread = 32;                     // per dequantising thread and stage
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
   static_assert(kRawRow == 32 || kRawRow == 64 || kRawRow == 128, "raw box width");
-  static_assert(kPfAStages * kPfAStageCols + kPfACol <= 512, "TMEM budget");
+  static_assert(kAStages * kAStageCols + kPfACol <= 512, "TMEM budget");
 };
 
 template <int QT, bool GU>
@@ -314,7 +319,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   constexpr bool I4 = QT == COLI_Q_INT4_G128;
   constexpr int S = L::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ uint64_t tma_full[S], tma_empty[S], a_full[kPfAStages], a_empty[kPfAStages], acc_full[2], acc_empty[2];
+  __shared__ uint64_t tma_full[S], tma_empty[S], a_full[kPfAStagesMax], a_empty[kPfAStagesMax], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -327,7 +332,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(&tma_full[s], 1);
       mbar_init(&tma_empty[s], 1);
     }
-    for (int s = 0; s < kPfAStages; ++s) {
+    for (int s = 0; s < L::kAStages; ++s) {
       mbar_init(&a_full[s], kPfDqWarps);
       mbar_init(&a_empty[s], 1);
     }
@@ -430,15 +435,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const uint32_t dacc = tmem + (uint32_t)(acc * 128);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % S, as = it % kPfAStages;
+          const int s = it % S, as = it % L::kAStages;
           // a_full also covers the stage's TMA data: every dequantising warp waited for
           // tma_full[s] (raw codes and activations share that barrier) before arriving
-          if (!mbar_wait_spin(&a_full[as], (it / kPfAStages) & 1)) { ok = false; break; }
+          if (!mbar_wait_spin(&a_full[as], (it / L::kAStages) & 1)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t A = tmem + (uint32_t)(kPfACol + as * kPfAStageCols);
+          const uint32_t A = tmem + (uint32_t)(kPfACol + as * L::kAStageCols);
           const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
-          if (GU) umma_stage_gu(dacc, A, bd, idesc, (uint32_t)kb);
-          else umma_stage_dn(dacc, A, bd, idesc, (uint32_t)kb, (uint32_t)(L::kBAtomBytes >> 4));
+          if (GU) {
+            // gate columns [0, K/2), up columns [K/2, K) of the stage; one B atom per 64 K
+#pragma unroll
+            for (int at = 0; at < L::kAtoms; ++at)
+              umma_stage_gu(dacc, A + at * 32, A + L::kStageK / 2 + at * 32, bd + (uint64_t)(at * (L::kBAtomBytes >> 4)),
+                            idesc, at == 0 ? (uint32_t)kb : 1u);
+          } else {
+            umma_stage_dn(dacc, A, bd, idesc, (uint32_t)kb, (uint32_t)(L::kBAtomBytes >> 4));
+          }
           umma_commit(&tma_empty[s]);
           umma_commit(&a_empty[as]);
         }
@@ -446,7 +458,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(&acc_full[acc]);
       }
       // wait for the MMAs in flight before the CTA releases TMEM
-      if (it > 0) mbar_wait(&a_empty[(it - 1) % kPfAStages], ((it - 1) / kPfAStages) & 1);
+      if (it > 0) mbar_wait(&a_empty[(it - 1) % L::kAStages], ((it - 1) / L::kAStages) & 1);
     }
   } else if (warp < 2 + kPfEpWarps) {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
@@ -501,13 +513,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- dequantise (warps 6..21)
-    // thread = (TMEM lane = weight row r, part g): 32 codes of row r per stage.
-    // gate/up: g -> (matrix g & 1, K half g >> 1); down: g -> K quarter.
+    // thread = (TMEM lane = weight row r, group g): per stage L::kParts parts of 32 codes of row r.
+    // gate/up: g -> matrix g & 1, K quarters 2*(g >> 1) and +1; down: g -> K quarter g.
     const int sp = warp & 3, r = sp * 32 + lane;
     const int g = (warp - 2 - kPfEpWarps) >> 2;      // 0..3
     const int mat_i = GU ? (g & 1) : 0;
-    const int kpart = GU ? (g >> 1) : g;
-    const uint32_t tcol = (uint32_t)(GU ? mat_i * 32 + kpart * 16 : kpart * 16);
+    const int kpart = GU ? (g >> 1) * L::kParts : g;  // first part
+    const uint32_t tcol = (uint32_t)(mat_i * (L::kStageK / 2) + kpart * 16);
     const uint32_t tlane = (uint32_t)(sp * 32) << 16;
     int it = 0;
     for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x) {
@@ -549,7 +561,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % S, as = it % kPfAStages;
+        const int s = it % S, as = it % L::kAStages;
         uint32_t ss = 0, zz = zz8, zzh = 0;
         if (I4) {
           uint32_t sraw, zraw;
@@ -575,37 +587,41 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           zzh = (0x5400u | (zraw << 4)) * 0x10001u;  // half2(64 + z)
         }
         if (!mbar_wait(&tma_full[s], (it / S) & 1)) { ok = false; break; }
-        if (it >= kPfAStages) {
-          if (!mbar_wait(&a_empty[as], ((it / kPfAStages) - 1) & 1)) { ok = false; break; }
+        if (it >= L::kAStages) {
+          if (!mbar_wait(&a_empty[as], ((it / L::kAStages) - 1) & 1)) { ok = false; break; }
           tc_fence_after();
         }
         const uint8_t* raw = smem + (size_t)s * L::kStageBytes + L::kBBytes + (GU ? mat_i * L::kRawBytes : 0) +
                              r * L::kRawRow;
-        uint32_t o[16];
-        if (I4) {
-          const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, kpart) << 4)));
-          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t q8 = qw[j] >> 8;
-            o[4 * j + 0] = h2_mul(h2_sub(nib_lo_h1024(qw[j]), zz), ss);
-            o[4 * j + 1] = h2_mul(h2_sub(nib_hi_h64(qw[j]), zzh), ss);
-            o[4 * j + 2] = h2_mul(h2_sub(nib_lo_h1024(q8), zz), ss);
-            o[4 * j + 3] = h2_mul(h2_sub(nib_hi_h64(q8), zzh), ss);
-          }
-        } else {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, 2 * kpart + h) << 4)));
+        for (int pp = 0; pp < L::kParts; ++pp) {
+          const int kp = kpart + pp;
+          uint32_t o[16];
+          if (I4) {
+            const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, kp) << 4)));
             const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              o[8 * h + 2 * j] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4140), zz);
-              o[8 * h + 2 * j + 1] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4342), zz);
+              const uint32_t q8 = qw[j] >> 8;
+              o[4 * j + 0] = h2_mul(h2_sub(nib_lo_h1024(qw[j]), zz), ss);
+              o[4 * j + 1] = h2_mul(h2_sub(nib_hi_h64(qw[j]), zzh), ss);
+              o[4 * j + 2] = h2_mul(h2_sub(nib_lo_h1024(q8), zz), ss);
+              o[4 * j + 3] = h2_mul(h2_sub(nib_hi_h64(q8), zzh), ss);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 q = lds128(smem_u32(raw + (swz_chunk<L::kRawRow>(r, 2 * kp + h) << 4)));
+              const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                o[8 * h + 2 * j] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4140), zz);
+                o[8 * h + 2 * j + 1] = h2_sub(__byte_perm(qw[j], 0x64646464u, 0x4342), zz);
+              }
             }
           }
+          tmem_st16(tmem + tlane + (uint32_t)(kPfACol + as * L::kAStageCols) + tcol + pp * 16, o);
         }
-        tmem_st16(tmem + tlane + (uint32_t)(kPfACol + as * kPfAStageCols) + tcol, o);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
