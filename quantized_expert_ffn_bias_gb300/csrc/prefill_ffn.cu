@@ -302,7 +302,8 @@ struct PfLayout {
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = kStages * kStageBytes;
   static constexpr int kAccSets = GU ? 1 : 2;                    // TMEM columns 0..255 hold the accumulators
-  static constexpr int kAStageCols = kMats * kStageK / 2;        // two fp16 per TMEM column
+  static constexpr int kTmaPerA = 1;                             // TMA stages per TMEM A stage
+  static constexpr int kAStageCols = kMats * kStageK * kTmaPerA / 2;  // two fp16 per TMEM column
   static constexpr int kAStages = 256 / kAStageCols;             // TMEM A ring depth
   static constexpr int kParts = kMats * kStageK / 32 / 4;        // 32-code parts per dequantising thread
   static_assert(kAStages <= kPfAStagesMax, "A ring");
@@ -419,11 +420,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int it = 0, tcount = 0;
+      int it = 0, ia = 0, tcount = 0;   // TMA stages, TMEM A stages, tiles
       for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x, ++tcount) {
         int slot, row0, ntok, mb, K;
         tile_info(t, slot, row0, ntok, mb, K);
-        const int nkb = K / L::kStageK;
+        const int ntma = K / L::kStageK, nA = (ntma + L::kTmaPerA - 1) / L::kTmaPerA;
         const int N = (ntok + 15) & ~15;
         const uint32_t idesc = umma_idesc_f16(kPfM, N);
         const int acc = GU ? 0 : (tcount & 1);
@@ -434,31 +435,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         }
         const uint32_t dacc = tmem + (uint32_t)(acc * 128);
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const int s = it % S, as = it % L::kAStages;
-          // a_full also covers the stage's TMA data: every dequantising warp waited for
-          // tma_full[s] (raw codes and activations share that barrier) before arriving
-          if (!mbar_wait_spin(&a_full[as], (it / L::kAStages) & 1)) { ok = false; break; }
+        for (int j = 0; j < nA; ++j, ++ia) {
+          const int as = ia % L::kAStages;
+          // a_full also covers the TMA data of the A stage's TMA stages: every dequantising warp
+          // waited for their tma_full (raw codes and activations share that barrier) before arriving
+          if (!mbar_wait_spin(&a_full[as], (ia / L::kAStages) & 1)) { ok = false; break; }
           tc_fence_after();
           const uint32_t A = tmem + (uint32_t)(kPfACol + as * L::kAStageCols);
-          const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
-          if (GU) {
-            // gate columns [0, K/2), up columns [K/2, K) of the stage; one B atom per 64 K
+          const int nsub = min(L::kTmaPerA, ntma - j * L::kTmaPerA);
+          for (int sub = 0; sub < nsub; ++sub, ++it) {
+            const int s = it % S;
+            const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
+            const uint32_t kbf = (j > 0 || sub > 0) ? 1u : 0u;   // 0: the tile's first MMAs overwrite
+            if (GU) {
+              // gate columns [0, K/2), up columns [K/2, K) of the stage; one B atom per 64 K
 #pragma unroll
-            for (int at = 0; at < L::kAtoms; ++at)
-              umma_stage_gu(dacc, A + at * 32, A + L::kStageK / 2 + at * 32, bd + (uint64_t)(at * (L::kBAtomBytes >> 4)),
-                            idesc, at == 0 ? (uint32_t)kb : 1u);
-          } else {
-            umma_stage_dn(dacc, A, bd, idesc, (uint32_t)kb, (uint32_t)(L::kBAtomBytes >> 4));
+              for (int at = 0; at < L::kAtoms; ++at)
+                umma_stage_gu(dacc, A + at * 32, A + L::kStageK / 2 + at * 32,
+                              bd + (uint64_t)(at * (L::kBAtomBytes >> 4)), idesc, at == 0 ? kbf : 1u);
+            } else {
+              umma_stage_dn(dacc, A + sub * (L::kStageK / 2), bd, idesc, kbf, (uint32_t)(L::kBAtomBytes >> 4));
+            }
+            umma_commit(&tma_empty[s]);
           }
-          umma_commit(&tma_empty[s]);
           umma_commit(&a_empty[as]);
         }
         if (!ok) { fail_wait(); break; }
         umma_commit(&acc_full[acc]);
       }
       // wait for the MMAs in flight before the CTA releases TMEM
-      if (it > 0) mbar_wait(&a_empty[(it - 1) % L::kAStages], ((it - 1) / L::kAStages) & 1);
+      if (ia > 0) mbar_wait(&a_empty[(ia - 1) % L::kAStages], ((ia - 1) / L::kAStages) & 1);
     }
   } else if (warp < 2 + kPfEpWarps) {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
@@ -521,7 +527,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int kpart = GU ? (g >> 1) * L::kParts : g;  // first part
     const uint32_t tcol = (uint32_t)(mat_i * (L::kStageK / 2) + kpart * 16);
     const uint32_t tlane = (uint32_t)(sp * 32) << 16;
-    int it = 0;
+    int it = 0, ia = 0;   // TMA stages, TMEM A stages
     for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x) {
       int slot, row0, ntok, mb, K;
       tile_info(t, slot, row0, ntok, mb, K);
@@ -560,8 +566,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         load_sz(0, s_next, z_next);
       }
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const int s = it % S, as = it % L::kAStages;
+      const int nA = (nkb + L::kTmaPerA - 1) / L::kTmaPerA;
+      for (int j = 0; j < nA && ok; ++j, ++ia) {
+        const int as = ia % L::kAStages;
+        if (ia >= L::kAStages) {
+          if (!mbar_wait(&a_empty[as], ((ia / L::kAStages) - 1) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
+        const int nsub = min(L::kTmaPerA, nkb - j * L::kTmaPerA);
+        for (int sub = 0; sub < nsub; ++sub, ++it) {
+        const int kb = j * L::kTmaPerA + sub, s = it % S;
         uint32_t ss = 0, zz = zz8, zzh = 0;
         if (I4) {
           uint32_t sraw, zraw;
@@ -587,10 +601,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           zzh = (0x5400u | (zraw << 4)) * 0x10001u;  // half2(64 + z)
         }
         if (!mbar_wait(&tma_full[s], (it / S) & 1)) { ok = false; break; }
-        if (it >= L::kAStages) {
-          if (!mbar_wait(&a_empty[as], ((it / L::kAStages) - 1) & 1)) { ok = false; break; }
-          tc_fence_after();
-        }
         const uint8_t* raw = smem + (size_t)s * L::kStageBytes + L::kBBytes + (GU ? mat_i * L::kRawBytes : 0) +
                              r * L::kRawRow;
 #pragma unroll
@@ -620,9 +630,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               }
             }
           }
-          tmem_st16(tmem + tlane + (uint32_t)(kPfACol + as * L::kAStageCols) + tcol + pp * 16, o);
+          tmem_st16(tmem + tlane + (uint32_t)(kPfACol + as * L::kAStageCols + sub * (L::kStageK / 2)) + tcol +
+                        pp * 16,
+                    o);
         }
-        tmem_st_wait();
+        }   // TMA stages of this A stage
+        __syncwarp();
+        tmem_st_wait();                 // also on the abort path: no store may be in flight at teardown
+        if (!ok) break;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[as]);
