@@ -30,9 +30,11 @@
 //
 // CTA (persistent, one per SM): warp 0 issues TMA loads (raw codes and
 // activation rows) into a ring of stages, with L2 prefetch of the codes further
-// ahead; warp 1 owns TMEM and issues the MMAs (one thread); warps 2..5 run the
-// epilogue; warps 6..21 dequantise into a 4-deep ring of TMEM A stages.  All
-// waits are bounded; a timeout sets the status word and every role stops.
+// ahead; warp 1 owns TMEM and issues the MMAs (one thread; for gate/up it
+// issues the gate matrix and warp 22 the up matrix: the issuing thread sets the
+// pace, and two of them on different sub-partitions issue more MMAs); warps
+// 2..5 run the epilogue; warps 6..21 dequantise into a ring of TMEM A stages.
+// All waits are bounded; a timeout sets the status word and every role stops.
 #include "moe_internal.cuh"
 
 namespace coli {
@@ -42,7 +44,8 @@ constexpr int kPfN = kPrefillChunk;  // tokens per chunk (largest MMA N)
 constexpr int kPfBBox = 64;         // activation rows per TMA box
 constexpr int kPfEpWarps = 4;       // epilogue warps (one per TMEM sub-partition)
 constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-partition)
-constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps) * 32;
+constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps + 1) * 32;   // + second MMA issuer (gate/up)
+constexpr int kPfIssuer2Warp = 2 + kPfEpWarps + kPfDqWarps;
 constexpr int kPfAStagesMax = 4;    // deepest TMEM A ring (barrier arrays)
 
 struct PfChunk { int slot, row0, ntok, pad; };
@@ -160,33 +163,12 @@ __device__ __forceinline__ uint32_t umma_idesc_f16(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// The eight K16 MMAs of one pipeline stage in one block: the issuing thread
-// is on the critical path of the tensor pipe, so it executes as few
-// instructions per MMA as possible.  `kb` is the stage's index within the
-// tile: stage 0 overwrites the accumulators, later stages add to them.
-// gate/up, four K16 steps of both matrices from one 128-byte B atom: gate A at
-// TMEM column a, up A at column a_up (each advancing 8 columns per step).
-__device__ __forceinline__ void umma_stage_gu(uint32_t d_gate, uint32_t a, uint32_t a_up, uint64_t b, uint32_t idesc,
-                                              uint32_t kb) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t.reg .b32 a0, a1, a2, a3, a4, a5, a6, a7, dup;\n\t.reg .b64 b1, b2, b3;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 q, 0, 0;\n\t"
-      "add.u32 dup, %0, 128;\n\t"
-      "mov.u32 a1, %5;\n\tadd.u32 a2, %1, 8;\n\tadd.u32 a3, %5, 8;\n\t"
-      "add.u32 a4, %1, 16;\n\tadd.u32 a5, %5, 16;\n\tadd.u32 a6, %1, 24;\n\tadd.u32 a7, %5, 24;\n\t"
-      "add.u64 b1, %2, 2;\n\tadd.u64 b2, %2, 4;\n\tadd.u64 b3, %2, 6;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a1], %2, %3, p;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b1, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a3], b1, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], b2, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a5], b2, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], b3, %3, q;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [dup], [a7], b3, %3, q;\n\t}" ::"r"(d_gate),
-      "r"(a), "l"(b), "r"(idesc), "r"(kb), "r"(a_up));
-}
-// down: A stage = K128 (64 columns), B = two 128-byte atoms 16 * atom16 bytes apart.
-__device__ __forceinline__ void umma_stage_dn(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb,
+// The eight K16 MMAs of one matrix and one K128 pipeline stage in one block:
+// A = 64 TMEM columns, B = two 128-byte atoms 16 * atom16 bytes apart.  The
+// issuing thread is on the critical path of the tensor pipe, so it executes as
+// few instructions per MMA as possible.  `kb` = 0 for the tile's first stage
+// (overwrite the accumulators), non-zero after (add to them).
+__device__ __forceinline__ void umma_k128(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t kb,
                                               uint32_t atom16) {
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t.reg .b64 b1, b2, b3, b4, b5, b6, b7, bb;\n\t"
@@ -329,16 +311,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   volatile int* abort_v = &abort_flag;
 
   if (threadIdx.x == 0) {
+    constexpr int NI = GU ? 2 : 1;   // MMA-issuing threads (each commits)
     for (int s = 0; s < S; ++s) {
       mbar_init(&tma_full[s], 1);
-      mbar_init(&tma_empty[s], 1);
+      mbar_init(&tma_empty[s], NI);
     }
     for (int s = 0; s < L::kAStages; ++s) {
       mbar_init(&a_full[s], kPfDqWarps);
-      mbar_init(&a_empty[s], 1);
+      mbar_init(&a_empty[s], NI);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&acc_full[s], 1);
+      mbar_init(&acc_full[s], NI);
       mbar_init(&acc_empty[s], kPfEpWarps);
     }
     abort_flag = 0;
@@ -417,8 +400,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int issued = it;
       for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_full[j % S], (j / S) & 1);
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || (GU && warp == kPfIssuer2Warp)) {
+    // ---------------------------------------------------------------- MMA issuers (gate/up: gate | up)
+    const int mi = warp == 1 ? 0 : 1;
     if (lane == 0) {
       int it = 0, ia = 0, tcount = 0;   // TMA stages, TMEM A stages, tiles
       for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x, ++tcount) {
@@ -448,13 +432,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
             const uint32_t kbf = (j > 0 || sub > 0) ? 1u : 0u;   // 0: the tile's first MMAs overwrite
             if (GU) {
-              // gate columns [0, K/2), up columns [K/2, K) of the stage; one B atom per 64 K
-#pragma unroll
-              for (int at = 0; at < L::kAtoms; ++at)
-                umma_stage_gu(dacc, A + at * 32, A + L::kStageK / 2 + at * 32,
-                              bd + (uint64_t)(at * (L::kBAtomBytes >> 4)), idesc, at == 0 ? kbf : 1u);
+              umma_k128(dacc + mi * 128, A + mi * (L::kStageK / 2), bd, idesc, kbf,
+                            (uint32_t)(L::kBAtomBytes >> 4));
             } else {
-              umma_stage_dn(dacc, A + sub * (L::kStageK / 2), bd, idesc, kbf, (uint32_t)(L::kBAtomBytes >> 4));
+              umma_k128(dacc, A + sub * (L::kStageK / 2), bd, idesc, kbf, (uint32_t)(L::kBAtomBytes >> 4));
             }
             umma_commit(&tma_empty[s]);
           }
@@ -517,7 +498,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[acc]);
     }
-  } else {
+  } else if (warp < kPfIssuer2Warp) {
     // ---------------------------------------------------------------- dequantise (warps 6..21)
     // thread = (TMEM lane = weight row r, group g): per stage L::kParts parts of 32 codes of row r.
     // gate/up: g -> matrix g & 1, K quarters 2*(g >> 1) and +1; down: g -> K quarter g.
