@@ -43,6 +43,31 @@ MEDIUM = [
 ]
 
 
+# tensor-core (T > 8) path: every output checked.  Covers shared experts with d_ff below and above the
+# routed one (the hidden row stride is the larger), int8 with a shared expert, int4 group counts that
+# are not multiples of 8 (per-stage scale loads instead of 8-group batches), token counts that are not
+# multiples of 16 (MMA N rounding) and experts with more than one 128-token chunk.
+PREFILL = [
+    # (qtype, d, F, E, k, F_shared, bias, T values)
+    (H.Q_INT4_G128, 1024, 512, 16, 4, 256, "uniform:0.1", (9, 130)),
+    (H.Q_INT4_G128, 768, 1280, 64, 6, 512, "zipf:0.05:1.1", (64, 300)),
+    (H.Q_INT8_PC, 640, 256, 32, 8, 384, "normal:0.5", (17, 200)),
+    (H.Q_INT4_G128, 2048, 1024, 8, 2, 1024, "spike:3:2.0", (257,)),
+]
+
+
+@pytest.mark.parametrize("case", range(len(PREFILL)))
+def test_prefill_shapes(case):
+    qt, d, F, E, k, Fs, bias, Ts = PREFILL[case]
+    layer = H.gen_layer(200 + case, 0, d=d, F=F, E=E, k=k, rho=2.5, qtype=qt, bias=bias, F_shared=Fs)
+    dl = _dl(layer, max(Ts))
+    for i, T in enumerate(Ts):
+        x = H.gen_x(200 + case, i, T, d, H.X_BF16)
+        rep = run_layer_parity(dl, layer, x)
+        assert rep.set_mismatch == 0 or rep.near_ties >= rep.set_mismatch
+    dl.close()
+
+
 @pytest.mark.parametrize("case", range(len(MEDIUM)))
 def test_medium_shapes(case):
     qt, d, F, E, k, Fs, bias, Ts = MEDIUM[case]
