@@ -40,7 +40,7 @@ enum KernelId {
   K_COMBINE, K_COUNT
 };
 const char* kKernelNames[K_COUNT] = {"route_decode", "router_logits",  "router_topk",    "permute",
-                                     "prep_xs",      "expert_gate_up", "expert_down",    "gather_x",
+                                     "quantize_h",   "expert_gate_up", "expert_down",    "gather_x",
                                      "plan_tiles",   "tc_gate_up",     "tc_down",        "combine"};
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -129,6 +129,8 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.xqs = take(T * (size_t)(d.d / kXqBlock) * 8);
   w.h = take(rows * (size_t)p->Fmax * 4);
   w.hsum = take(rows * (size_t)(p->Fmax / 8) * 4);
+  w.hq = take(rows * (size_t)p->Fmax * 2);
+  w.hqs = take(rows * (size_t)(p->Fmax / kXqBlock) * 8);
   w.y = take(rows * (size_t)d.d * 4);
   w.xh = w.chunks = w.gu_tiles = w.dn_tiles = w.pf_counts = 0;
   if (d.T_max > kDecodeMaxT) {
@@ -295,6 +297,8 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   a.xqs = reinterpret_cast<int2*>(ws + w.xqs);
   a.h = reinterpret_cast<float*>(ws + w.h);
   a.hsum = reinterpret_cast<float*>(ws + w.hsum);
+  a.hq = reinterpret_cast<uint32_t*>(ws + w.hq);
+  a.hqs = reinterpret_cast<int2*>(ws + w.hqs);
   a.y = reinterpret_cast<float*>(ws + w.y);
 
   const bool prof = plan->prof_calls < plan->prof_max_calls;
@@ -333,6 +337,9 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   if (T <= kDecodeMaxT) {
     if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
       return cuda_fail(ce, "forward: expert_gate_up");
+    if (d.qtype == COLI_Q_INT4_G128 &&
+        (ce = run(K_PREP, [&] { return launch_quantize_h(a, st); })) != cudaSuccess)
+      return cuda_fail(ce, "forward: quantize_h");
     if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)
       return cuda_fail(ce, "forward: expert_down");
   } else {

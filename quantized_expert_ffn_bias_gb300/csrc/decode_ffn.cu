@@ -21,8 +21,8 @@
 //
 // int4 (integer dot products): the activations enter in 16-bit fixed point per
 // block of 32 inputs, x = sx*(256*hi + lo) with hi a signed and lo an unsigned
-// byte.  gate/up: prepared once per token by the routing kernel; down: each
-// lane converts its own 32 hidden values (one block) per stage.  Masking a word
+// byte, prepared once per token (gate/up: by the routing kernel) or per pair row
+// (down: by quantize_h after the gate/up kernel).  Masking a word
 // of codes and its 4-bit shift with 0x0F0F0F0F gives the even and odd codes as
 // bytes, so one 8-code word costs three logic ops and four dp4a; sum(c*q) and
 // z*sum(q) are exact integers and one conversion per 32 codes brings them to
@@ -260,43 +260,6 @@ __device__ __forceinline__ int dot_row_int4_dp4a(uint4 w, const uint32_t (&xh)[8
   return hi * 256 + (int)lo;
 }
 
-// 32 fp32 values (a lane's block) -> fixed point in the dot-product layout:
-// sx = 2^(floor(log2 max|v|) - 14), q = rint(v / sx) (|q| <= 32767).
-__device__ __forceinline__ void quantize32(const ulonglong2 (&v)[8], uint32_t (&xh)[8], uint32_t (&xl)[8], float& sx,
-                                           int& qsum) {
-  float f[32];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    f[4 * i] = __uint_as_float((uint32_t)v[i].x);
-    f[4 * i + 1] = __uint_as_float((uint32_t)(v[i].x >> 32));
-    f[4 * i + 2] = __uint_as_float((uint32_t)v[i].y);
-    f[4 * i + 3] = __uint_as_float((uint32_t)(v[i].y >> 32));
-  }
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(f[i]));
-  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
-  e = e < -100 ? -100 : e;
-  sx = __uint_as_float((uint32_t)(e - 14 + 127) << 23);
-  const float inv = __uint_as_float((uint32_t)(14 - e + 127) << 23);
-  int q[32];
-  qsum = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    q[i] = min(__float2int_rn(f[i] * inv), 32767);
-    qsum += q[i];
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-#pragma unroll
-    for (int od = 0; od < 2; ++od) {
-      const int* b = q + 8 * j + od;   // inputs 8j+od, +2, +4, +6
-      xh[2 * j + od] = __byte_perm(__byte_perm(b[0], b[2], 0x0051), __byte_perm(b[4], b[6], 0x0051), 0x5410);
-      xl[2 * j + od] = __byte_perm(__byte_perm(b[0], b[2], 0x0040), __byte_perm(b[4], b[6], 0x0040), 0x5410);
-    }
-  }
-}
-
 __device__ __forceinline__ float pair_sum(uint64_t p) {
   return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
 }
@@ -423,6 +386,8 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
     if (DOWN) {
       xrow[t] = a.h + (size_t)(p0 + tt) * a.Fmax;
       srow[t] = a.hsum + (size_t)(p0 + tt) * (a.Fmax / 8);
+      qrow[t] = a.hq + (size_t)(p0 + tt) * (a.Fmax / 2);
+      qsrow[t] = a.hqs + (size_t)(p0 + tt) * (a.Fmax / kXqBlock);
     } else {
       const int tok = a.pair_token[p0 + tt];
       xrow[t] = a.xs + (size_t)tok * a.d;
@@ -437,7 +402,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
   };
   auto load_x = [&](int t, int code0, ulonglong2 (&xq)[8], float& xsum) {
     const int c = code0 < 0 ? 0 : code0;
-    if constexpr (DP && !DOWN) {   // 64 bytes of hi/lo words (as 4 x 16 bytes) and the block's (sx, sum q)
+    if constexpr (DP) {   // 64 bytes of hi/lo words (as 4 x 16 bytes) and the block's (sx, sum q)
       const int b = c / kXqBlock;
       const ulonglong2* src = reinterpret_cast<const ulonglong2*>(qrow[t] + (size_t)b * 16);
 #pragma unroll
@@ -448,8 +413,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
     } else {
 #pragma unroll
       for (int i = 0; i < XQ; ++i) xq[i] = ldg_nc_u64x2(xrow[t] + c + 4 * i);
-    if constexpr (DP) {  // int4 down: the block is converted where it is used
-    } else if (DOWN) {   // sums of h over 8 consecutive inputs
+    if (DOWN) {          // sums of h over 8 consecutive inputs
       if (I4) {
         const float4 h4 = __ldg(reinterpret_cast<const float4*>(srow[t] + c / 8));
         xsum = (h4.x + h4.y) + (h4.z + h4.w);
@@ -528,19 +492,15 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
           uint32_t xh[8], xl[8];
           float sx;
           int qsum;
-          if constexpr (DOWN) {
-            quantize32(xq, xh, xl, sx, qsum);
-          } else {
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              xh[4 * i] = (uint32_t)xq[i].x; xh[4 * i + 1] = (uint32_t)(xq[i].x >> 32);
-              xh[4 * i + 2] = (uint32_t)xq[i].y; xh[4 * i + 3] = (uint32_t)(xq[i].y >> 32);
-              xl[4 * i] = (uint32_t)xq[2 + i].x; xl[4 * i + 1] = (uint32_t)(xq[2 + i].x >> 32);
-              xl[4 * i + 2] = (uint32_t)xq[2 + i].y; xl[4 * i + 3] = (uint32_t)(xq[2 + i].y >> 32);
-            }
-            sx = __uint_as_float((uint32_t)xq[4].x);
-            qsum = (int)(uint32_t)(xq[4].x >> 32);
+          for (int i = 0; i < 2; ++i) {
+            xh[4 * i] = (uint32_t)xq[i].x; xh[4 * i + 1] = (uint32_t)(xq[i].x >> 32);
+            xh[4 * i + 2] = (uint32_t)xq[i].y; xh[4 * i + 3] = (uint32_t)(xq[i].y >> 32);
+            xl[4 * i] = (uint32_t)xq[2 + i].x; xl[4 * i + 1] = (uint32_t)(xq[2 + i].x >> 32);
+            xl[4 * i + 2] = (uint32_t)xq[2 + i].y; xl[4 * i + 3] = (uint32_t)(xq[2 + i].y >> 32);
           }
+          sx = __uint_as_float((uint32_t)xq[4].x);
+          qsum = (int)(uint32_t)(xq[4].x >> 32);
 #pragma unroll
           for (int r = 0; r < kRows; ++r) {
             const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));

@@ -72,6 +72,8 @@ struct WsLayout {
   size_t xqs;          // int2 [T_max][d / kXqBlock]  (block scale bits, sum of the fixed-point values)
   size_t h;            // float [P_max + T_max][Fmax]  (pre-scaled SwiGLU output)
   size_t hsum;         // float [P_max + T_max][Fmax / 8]  (unscaled sums of h over 8 rows)
+  size_t hq;           // uint32 [P_max + T_max][Fmax / 2]  h in the fixed-point layout of xq (int4 decode)
+  size_t hqs;          // int2 [P_max + T_max][Fmax / kXqBlock]
   size_t y;            // float [P_max + T_max][d]
   // tensor-core path (T_max > kDecodeMaxT only; 0 otherwise)
   size_t xh;           // fp16 [P_max + T_max][d]  activations in grouped order
@@ -112,6 +114,8 @@ struct FwdArgs {
   int2* xqs;                  // per block of kXqBlock inputs: (block scale bits, sum of the fixed-point values)
   float* h;
   float* hsum;
+  uint32_t* hq;
+  int2* hqs;
   float* y;
 };
 
@@ -122,6 +126,7 @@ cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_decode_down(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_combine(const FwdArgs& a, cudaStream_t st);
@@ -233,6 +238,29 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
     if (mbar_test_wait(bar, parity)) return true;
     if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
   }
+}
+
+// One warp converts a block of kXqBlock = 32 values (lane i holds value i) to
+// the fixed-point layout described at kXqBlock: 64 bytes at dst and
+// (sx bits, sum of q) at *qs.  sx = 2^(floor(log2 max|v|) - 14).
+__device__ __forceinline__ void warp_quantize_block32(float v, uint8_t* dst, int2* qs) {
+  const int lane = threadIdx.x & 31;
+  float m = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+  e = e < -100 ? -100 : e;                       // tiny blocks
+  const float sx = __uint_as_float((uint32_t)(e - 14 + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(14 - e + 127) << 23);
+  int q = __float2int_rn(v * inv);
+  q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
+  int sum = q;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  const int j = lane & 7, wd = (lane >> 3) * 2 + (j & 1);
+  dst[wd * 4 + (j >> 1)] = (uint8_t)((q >> 8) & 255);          // hi (two's complement byte)
+  dst[32 + wd * 4 + (j >> 1)] = (uint8_t)(q & 255);             // lo
+  if (lane == 0) *qs = make_int2(__float_as_int(sx), sum);
 }
 
 // Programmatic dependent launch: a kernel launched with launch_pdl may start

@@ -117,4 +117,34 @@ cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------ int4 decode: h -> fixed point
+// The SwiGLU outputs of every grouped pair row (valid columns: F, or F_shared
+// for the shared expert's rows) in the fixed-point layout the int4 down kernel
+// reads, one warp per block of 32 hidden units.
+__global__ void __launch_bounds__(256) quantize_h_kernel(FwdArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();                  // h of the gate/up kernel
+  const int P = a.T * a.k, rows = P + (a.has_shared ? a.T : 0), bpr = a.Fmax / kXqBlock;
+  const int lane = threadIdx.x & 31;
+  const long long nb = (long long)rows * bpr;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long b = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; b < nb; b += nw) {
+    const int r = (int)(b / bpr), c = (int)(b % bpr) * kXqBlock;
+    if (c >= (r >= P ? a.Fs : a.F)) continue;          // warp-uniform
+    const float v = a.h[(size_t)r * a.Fmax + c + lane];
+    warp_quantize_block32(v, reinterpret_cast<uint8_t*>(a.hq + (size_t)r * (a.Fmax / 2)) + (size_t)(c / kXqBlock) * 64,
+                          a.hqs + (size_t)r * bpr + c / kXqBlock);
+  }
+}
+
+cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st) {
+  const int rows = a.T * a.k + (a.has_shared ? a.T : 0);
+  const long long warps = (long long)rows * (a.Fmax / kXqBlock);
+  int blocks = (int)((warps + 7) / 8);
+  if (blocks > 1024) blocks = 1024;
+  if (blocks < 1) blocks = 1;
+  const cudaError_t e = launch_pdl(quantize_h_kernel, dim3(blocks), dim3(256), 0, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 }  // namespace coli

@@ -378,24 +378,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
       const int i = b * kXqBlock + lane;
       const float v = XT == COLI_X_BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16)
                                         : static_cast<const float*>(a.x)[i];
-      float m = fabsf(v);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      // sx = 2^(floor(log2 m) - 14), so that |v| / sx < 2^15 (exponent clamped for tiny blocks)
-      int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
-      e = e < -100 ? -100 : e;
-      const float sx = __uint_as_float((uint32_t)(e - 14 + 127) << 23);
-      const float inv = __uint_as_float((uint32_t)(14 - e + 127) << 23);
-      int q = __float2int_rn(v * inv);
-      q = q > 32767 ? 32767 : (q < -32767 ? -32767 : q);
-      int qs = q;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) qs += __shfl_xor_sync(0xffffffffu, qs, o);
-      uint8_t* dst = reinterpret_cast<uint8_t*>(a.xq) + (size_t)b * 64;
-      const int j = lane & 7, wd = (lane >> 3) * 2 + (j & 1);
-      dst[wd * 4 + (j >> 1)] = (uint8_t)((q >> 8) & 255);          // hi (two's complement byte)
-      dst[32 + wd * 4 + (j >> 1)] = (uint8_t)(q & 255);             // lo
-      if (lane == 0) a.xqs[b] = make_int2(__float_as_int(sx), qs);
+      warp_quantize_block32(v, reinterpret_cast<uint8_t*>(a.xq) + (size_t)b * 64, a.xqs + b);
     }
   } else {
     const int n = a.T * a.d;
