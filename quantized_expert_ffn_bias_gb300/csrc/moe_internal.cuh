@@ -148,7 +148,10 @@ cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void
 constexpr int kXqBlock = 32;
 
 constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box height of the raw-code maps)
-constexpr int kPrefillChunk = 128;  // tokens per chunk (largest MMA N)
+#ifndef COLI_PREFILL_CHUNK
+#define COLI_PREFILL_CHUNK 128
+#endif
+constexpr int kPrefillChunk = COLI_PREFILL_CHUNK;  // tokens per chunk (largest MMA N): 64 or 128
 
 // K extent of one pipeline stage of the tensor-core path (128: one int4 group
 // per stage; gate/up stages carry both matrices).  The raw-code TMA box of a

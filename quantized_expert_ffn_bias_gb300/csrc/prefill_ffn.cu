@@ -46,7 +46,7 @@ constexpr int kPfEpWarps = 4;       // epilogue warps (one per TMEM sub-partitio
 constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-partition)
 constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps + 1) * 32;   // + second MMA issuer (gate/up)
 constexpr int kPfIssuer2Warp = 2 + kPfEpWarps + kPfDqWarps;
-constexpr int kPfAStagesMax = 4;    // deepest TMEM A ring (barrier arrays)
+constexpr int kPfAStagesMax = 8;    // deepest TMEM A ring (barrier arrays)
 
 struct PfChunk { int slot, row0, ntok, pad; };
 struct PfTile { int chunk, mb, pad0, pad1; };
@@ -268,7 +268,10 @@ struct PfArgs {
   float* yout;                 // down: Y [rows][d] fp32
 };
 
-constexpr int kPfACol = 256;        // first TMEM column of the A ring (columns 256..511)
+// TMEM: accumulators in columns [0, 2 * kPfN) (gate/up: gate and up of one
+// tile; down: two tiles, double-buffered), then the ring of A stages
+constexpr int kPfACol = 2 * kPfN;
+static_assert(kPfN == 64 || kPfN == 128, "chunk size");
 
 template <int QT, bool GU>
 struct PfLayout {
@@ -286,7 +289,7 @@ struct PfLayout {
   static constexpr int kAccSets = GU ? 1 : 2;                    // TMEM columns 0..255 hold the accumulators
   static constexpr int kTmaPerA = 1;                             // TMA stages per TMEM A stage
   static constexpr int kAStageCols = kMats * kStageK * kTmaPerA / 2;  // two fp16 per TMEM column
-  static constexpr int kAStages = 256 / kAStageCols;             // TMEM A ring depth
+  static constexpr int kAStages = (512 - kPfACol) / kAStageCols;   // TMEM A ring depth
   static constexpr int kParts = kMats * kStageK / 32 / 4;        // 32-code parts per dequantising thread
   static_assert(kAStages <= kPfAStagesMax, "A ring");
   static constexpr int kCodesPerThread = 32;                     // per dequantising thread and stage
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           if (!mbar_wait_spin(&acc_empty[acc], (uses - 1) & 1)) { fail_wait(); break; }
           tc_fence_after();
         }
-        const uint32_t dacc = tmem + (uint32_t)(acc * 128);
+        const uint32_t dacc = tmem + (uint32_t)(acc * kPfN);
         bool ok = true;
         for (int j = 0; j < nA; ++j, ++ia) {
           const int as = ia % L::kAStages;
@@ -432,7 +435,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             const uint64_t bd = umma_desc_sw128(smem_u32(smem + (size_t)s * L::kStageBytes));
             const uint32_t kbf = (j > 0 || sub > 0) ? 1u : 0u;   // 0: the tile's first MMAs overwrite
             if (GU) {
-              umma_k128(dacc + mi * 128, A + mi * (L::kStageK / 2), bd, idesc, kbf,
+              umma_k128(dacc + mi * kPfN, A + mi * (L::kStageK / 2), bd, idesc, kbf,
                             (uint32_t)(L::kBAtomBytes >> 4));
             } else {
               umma_k128(dacc, A + sub * (L::kStageK / 2), bd, idesc, kbf, (uint32_t)(L::kBAtomBytes >> 4));
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tc_fence_after();
       const DevExpert& ex = a.experts[slot];
       const int orow = mb * kPfM + sp * 32 + lane;  // weight row of this thread (TMEM lane)
-      const uint32_t lane_addr = tmem + ((uint32_t)(sp * 32) << 16) + (uint32_t)(acc * 128);
+      const uint32_t lane_addr = tmem + ((uint32_t)(sp * 32) << 16) + (uint32_t)(acc * kPfN);
       float s0 = 1.f, s1 = 1.f;
       if (!I4) {
         s0 = __ldg(static_cast<const float*>(ex.m[GU ? 0 : 2].s) + orow);
@@ -474,7 +477,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld16_issue(lane_addr + g16 * 16, r0);
         if (GU) {
           uint32_t r1[16];
-          tmem_ld16_issue(lane_addr + 128 + g16 * 16, r1);
+          tmem_ld16_issue(lane_addr + kPfN + g16 * 16, r1);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
