@@ -133,7 +133,14 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_086_912 + 2_788_352
+DECODE_GATEUP_T1_TRAFFIC = 122_094_080 + 3_076_864
+
+# DRAM bytes per launch of the prefill gate/up grouped GEMM at T=2048, E=256, scaled from the capture
+# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,751,424 B read + 17,507,072 B
+# written).  Both the expert bytes and the gathered activations grow with E and T by the same factor 4
+# (the one shared expert does not: 15 MB of the 4.3 GB); the full-size launch is too large to capture
+# with more than a one-pass metric.  None whenever that kernel changes.
+PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_067_751_424 + 17_507_072)
 
 
 def max_over_ranks(v: float, device=None) -> float:
@@ -259,7 +266,8 @@ def bench_native(args, rank: int, world: int):
             ach_d = dfl / (td_ms / td_n * 1e-3) / 1e12 if td_n else None
             layer_tf = (gfl + dfl) / (ms_tot / K * 1e-3) / 1e12
             roof = {"bound": "tensor", "kernel": "tc_gate_up", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
-                    "frac": (ach / pk_t) if ach else None, "traffic": None,
+                    "frac": (ach / pk_t) if ach else None,
+                    "traffic": PREFILL_GATEUP_T2048_TRAFFIC if (T == 2048 and not args.experts) else None,
                     "peak_source": pk["source"] + " (bf16 dense, sustained; fp16 runs at the same rate)",
                     "algorithmic_flops_per_launch": gfl, "down_kernel_achieved_tflops": ach_d,
                     "layer_tflops": layer_tf, "layer_frac_of_burst_peak": layer_tf / pk["bf16_tflops"]}
