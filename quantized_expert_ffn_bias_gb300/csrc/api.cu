@@ -354,7 +354,7 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
     {
       const cuuint64_t gdim[2] = {(cuuint64_t)d.d, (cuuint64_t)rows};
       const cuuint64_t gstr[1] = {(cuuint64_t)d.d * 2};
-      const cuuint32_t box[2] = {64, 64};
+      const cuuint32_t box[2] = {64, (cuuint32_t)kPrefillBBox};   // 128 bytes x kPrefillBBox rows
       const cuuint32_t es[2] = {1, 1};
       CUresult r = encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, xh, gdim, gstr, box, es,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

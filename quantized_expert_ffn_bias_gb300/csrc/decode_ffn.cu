@@ -573,7 +573,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   const int n_routed = a.n_unique[0];
   const int n_units = n_units_of<DOWN>(a, n_routed);
   const int stride = gridDim.x * kDecodeWarps;
-  const int first = blockIdx.x * kDecodeWarps + warp;
+  // units are dealt warp-major over the CTAs, so that a last, partial round of units keeps
+  // every SM streaming (5 or 6 warps each) instead of filling some SMs and idling others
+  const int first = warp * gridDim.x + blockIdx.x;
   if (first >= n_units) return;
 
   if (lane == 0) {

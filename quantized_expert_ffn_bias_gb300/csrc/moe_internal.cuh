@@ -152,6 +152,15 @@ constexpr int kPrefillRows = 128;   // weight rows per tensor-core tile (box hei
 #define COLI_PREFILL_CHUNK 128
 #endif
 constexpr int kPrefillChunk = COLI_PREFILL_CHUNK;  // tokens per chunk (largest MMA N): 64 or 128
+// Activation rows per TMA box of the tensor-core kernels (a chunk of n tokens loads
+// ceil(n / kPrefillBBox) boxes per 64-column atom).  Each TMA instruction costs the
+// single producer thread far more than the rows it moves: 64-row boxes measured
+// faster than 16-row boxes, which load only the rows the MMAs read.
+#ifndef COLI_PREFILL_BBOX
+#define COLI_PREFILL_BBOX 64
+#endif
+constexpr int kPrefillBBox = COLI_PREFILL_BBOX;
+static_assert(kPrefillBBox % 16 == 0 && kPrefillBBox <= kPrefillChunk && kPrefillBBox <= 256, "activation box");
 
 // K extent of one pipeline stage of the tensor-core path (128: one int4 group
 // per stage; gate/up stages carry both matrices).  The raw-code TMA box of a

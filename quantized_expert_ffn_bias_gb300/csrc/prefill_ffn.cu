@@ -43,7 +43,7 @@ namespace coli {
 
 constexpr int kPfM = 128;           // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kPfN = kPrefillChunk;  // tokens per chunk (largest MMA N)
-constexpr int kPfBBox = 64;         // activation rows per TMA box
+constexpr int kPfBBox = kPrefillBBox;   // activation rows per TMA box
 constexpr int kPfEpWarps = 4;       // epilogue warps (one per TMEM sub-partition)
 constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-partition)
 constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps + 1) * 32;   // + second MMA issuer (gate/up)
