@@ -133,14 +133,14 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_094_080 + 3_076_864
+DECODE_GATEUP_T1_TRAFFIC = 122_084_864 + 3_321_856
 
 # DRAM bytes per launch of the prefill gate/up grouped GEMM at T=2048, E=256, scaled from the capture
-# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,751,424 B read + 17,507,072 B
+# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,090,944 B read + 17,734,656 B
 # written).  Both the expert bytes and the gathered activations grow with E and T by the same factor 4
 # (the one shared expert does not: 15 MB of the 4.3 GB); the full-size launch is too large to capture
 # with more than a one-pass metric.  None whenever that kernel changes.
-PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_067_751_424 + 17_507_072)
+PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_067_090_944 + 17_734_656)
 
 
 def max_over_ranks(v: float, device=None) -> float:
