@@ -115,6 +115,42 @@ def workload_setup(name: str, experts: int = 0, tokens: int = 0):
     return w, Ts[0], Ts
 
 
+def qmat_bytes(qtype: int, N: int, K: int) -> int:
+    """Packed bytes of one [N][K] expert matrix: int4-g128 codes + fp16 scales + zero-point nibbles,
+    or int8 codes + fp32 scale + uint8 zero point per row."""
+    if qtype == H.Q_INT4_G128:
+        G = K // 128
+        return N * K // 2 + N * G * 2 + N * ((G + 1) // 2)
+    return N * K + N * 4 + N
+
+
+def expert_set_bytes(w) -> int:
+    """Bytes of all experts of every layer of workload w (routed and shared), as resident in HBM."""
+    total = 0
+    for qt in w.qtypes:
+        per = 2 * qmat_bytes(qt, w.F, w.d) + qmat_bytes(qt, w.d, w.F)
+        total += w.E * per
+        if w.F_shared:
+            total += 2 * qmat_bytes(qt, w.F_shared, w.d) + qmat_bytes(qt, w.d, w.F_shared)
+    return total
+
+
+def workload_config(w, T: int, world: int) -> dict:
+    """The JSON line's `config`: the workload alone (both arms print the same one)."""
+    if w.n_layers > 1:
+        return {"workload": f"stacked: {w.n_layers} GLM-5.2-class MoE layers (int4, int8 alternating) with "
+                            f"RMSNorm and residual, T={T} tokens per step",
+                "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho, "layers": w.n_layers,
+                "parallelism": "replicas" if world > 1 else "single GPU",
+                "l2": "inputs larger than L2: expert set of %.1f GB, fresh x every step" % (expert_set_bytes(w) / 1e9)}
+    return {"workload": f"{w.name}: GLM-5.2-class MoE layer, T={T} tokens per step",
+            "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho,
+            "qtype": "int4-g128" if w.qtypes[0] == H.Q_INT4_G128 else "int8-pc",
+            "shared_expert_d_ff": w.F_shared, "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2: expert set of %.2f GB, fresh x (fresh routing) every step"
+                  % (expert_set_bytes(w) / 1e9)}
+
+
 def unique_expert_bytes(dl, T) -> tuple[int, int]:
     """(gate+up bytes, down bytes) streamed by the last forward: unique routed experts + shared."""
     idx = dl.routing(T)[0]
@@ -180,9 +216,6 @@ def bench_native(args, rank: int, world: int):
     layer = w.layer(0)
     dl = DeviceLayer(layer, max(Ts), device=dev)
     gen_s = time.time() - t0
-    set_bytes = layer.experts.gate.nbytes + layer.experts.up.nbytes + layer.experts.down.nbytes
-    if layer.shared is not None:
-        set_bytes += layer.shared.gate.nbytes + layer.shared.up.nbytes + layer.shared.down.nbytes
     stream = torch.cuda.current_stream(dev)
     K, W = args.steps, args.warmup
     pk = peaks()
@@ -295,7 +328,7 @@ def bench_native(args, rank: int, world: int):
             "gpu_launches": K * r["launches"],
             "clocks": r["clocks"],
         }
-    return w, T_main, Ts, lines, gen_s, set_bytes
+    return w, T_main, Ts, lines, gen_s
 
 
 def bench_stacked(args, world: int):
@@ -321,7 +354,6 @@ def bench_stacked(args, world: int):
         dls.append((dl, layer.E, layer.k))
         del layer
     gen_s = time.time() - t0
-    set_bytes = sum(b * e for (b, _), (_, e, _) in zip(expert_bytes, dls))
     stream = torch.cuda.current_stream(dev)
     eps = w.rmsnorm_eps
     K, W = args.steps, args.warmup
@@ -411,12 +443,8 @@ def bench_stacked(args, world: int):
         "n_gpus": world, "steps": K, "warmup": W, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4/int8-weights, fp16 tensor-core operands, f32 accumulate",
         "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
-        "config": {"workload": f"stacked: 6 GLM-5.2-class MoE layers (int4, int8 alternating) with RMSNorm and "
-                               f"residual, T={T} tokens per step",
-                   "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho, "layers": w.n_layers,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: expert set of %.1f GB, fresh x every step" % (set_bytes / 1e9),
-                   "host_generation_s": round(gen_s, 1)},
+        "config": workload_config(w, T, world),
+        "host_generation_s": round(gen_s, 1),
         "cpu_baseline": None,
     }
     return line
@@ -478,12 +506,12 @@ def main():
         dt = time.perf_counter() - t0
         v = args.steps * n_tok / dt
         sample = f"{n_tok} tokens per step of the {w.name} workload, {cores} threads"
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 0,
+        # n_gpus: the launch's N (the oracle itself runs on the host cores, as cpu_baseline says)
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
                           "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                           "data": "synthetic",
-                          "config": {"workload": f"{w.name} (T={T_main})", "d": w.d, "d_ff": w.F, "E": w.E,
-                                     "k": w.k},
+                          "config": workload_config(w, T_main, world),
                           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                            "sample": sample},
                           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
@@ -499,7 +527,7 @@ def main():
         if rank == 0:
             print(json.dumps(line))
         return
-    w, T_main, Ts, lines, gen_s, set_bytes = bench_native(args, rank, world)
+    w, T_main, Ts, lines, gen_s = bench_native(args, rank, world)
     if rank != 0:
         return
     line = dict(lines[T_main])
@@ -510,13 +538,8 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int4-weights/f32-accumulate" if w.qtypes[0] == 0 else "int8",
         "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
-        "config": {"workload": f"{w.name}: GLM-5.2-class MoE layer, T={T_main} tokens per step",
-                   "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "routed_scale": w.rho,
-                   "qtype": "int4-g128" if w.qtypes[0] == 0 else "int8-pc",
-                   "shared_expert_d_ff": w.F_shared, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2: expert set of %.2f GB, fresh x (fresh routing) every step"
-                         % (set_bytes / 1e9),
-                   "host_generation_s": round(gen_s, 1)},
+        "config": workload_config(w, T_main, world),
+        "host_generation_s": round(gen_s, 1),
         "cpu_baseline": cpu,
     })
     line["variants"] = {f"T={T}": {k: lines[T][k] for k in ("value", "ms_per_step", "hbm_gbs_layer",
