@@ -330,6 +330,16 @@ __device__ __forceinline__ ScaleRaw load_scales_int4(const DevExpert& ex, const 
   const uint16_t* s = static_cast<const uint16_t*>(M.s) + (size_t)row * G + g0;
   const uint8_t* z = M.z + (size_t)row * ((G + 1) / 2) + g0 / 2;
   ScaleRaw o;
+  if ((G & 3) == 0 && (reinterpret_cast<uintptr_t>(M.s) & 7) == 0 && (reinterpret_cast<uintptr_t>(M.z) & 1) == 0 &&
+      g0 < G) {
+    // the lane's four scales are 8 aligned bytes and its four zero-point nibbles 2 aligned bytes:
+    // two loads instead of six (these loads sit on every stage of every warp)
+    const uint2 s4 = __ldg(reinterpret_cast<const uint2*>(s));
+    o.s01 = s4.x;
+    o.s23 = s4.y;
+    o.z4 = __ldg(reinterpret_cast<const uint16_t*>(z));
+    return o;
+  }
   uint32_t sv[4], zv[2];
 #pragma unroll
   for (int i = 0; i < 4; ++i) sv[i] = g0 + i < G ? __ldg(s + i) : 0u;
