@@ -169,7 +169,7 @@ def unique_expert_bytes(dl, T) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_084_864 + 3_321_856
+DECODE_GATEUP_T1_TRAFFIC = 122_086_656 + 3_052_288
 
 # DRAM bytes per launch of the prefill gate/up grouped GEMM at T=2048, E=256, scaled from the capture
 # summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,090,944 B read + 17,734,656 B
