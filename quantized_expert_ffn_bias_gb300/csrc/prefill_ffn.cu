@@ -34,6 +34,9 @@
 // issues the gate matrix and warp 22 the up matrix: the issuing thread sets the
 // pace, and two of them on different sub-partitions issue more MMAs); warps
 // 2..5 run the epilogue; warps 6..21 dequantise into a ring of TMEM A stages.
+// When every chunk has an even number of 128-row blocks, the CTAs launch as
+// clusters of two that run adjacent row blocks of the same chunk in lockstep
+// and share each stage's activation tiles by TMA multicast (see prefill_ffn_kernel).
 // All waits are bounded; a timeout sets the status word and every role stops.
 #include <algorithm>
 
