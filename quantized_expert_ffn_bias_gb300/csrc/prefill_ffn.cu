@@ -39,6 +39,7 @@
 // and share each stage's activation tiles by TMA multicast (see prefill_ffn_kernel).
 // All waits are bounded; a timeout sets the status word and every role stops.
 #include <algorithm>
+#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -722,13 +723,15 @@ static cudaError_t launch_pf(const FwdArgs& a, const PfArgs& p, const CUtensorMa
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    static int max_clusters = 0;   // co-resident clusters of this kernel (one device per process)
+    static std::atomic<int> cached{0};   // co-resident clusters of this kernel (one device per process)
+    int max_clusters = cached.load(std::memory_order_relaxed);
     if (max_clusters == 0) {
       int n = 0;
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
         cudaGetLastError();
         n = -1;
       }
+      cached.store(n, std::memory_order_relaxed);
       max_clusters = n;
     }
     if (max_clusters > 0) {
