@@ -21,9 +21,8 @@ COLI_Q_INT4_G128, COLI_Q_INT8_PC = 0, 1
 COLI_X_BF16, COLI_X_F32 = 0, 1
 COLI_DEV_BAD_EXPERT_ID, COLI_DEV_WAIT_TIMEOUT = 1, 2
 
-# COLIBRI_MOE_LIB selects another build of the library (for example a variant
-# compiled with different tuning switches); default: the in-tree build
-LIB_PATH = os.environ.get("COLIBRI_MOE_LIB") or _build.LIB
+# the in-tree build, the only library this binding loads
+LIB_PATH = _build.LIB
 _lock = threading.Lock()
 _lib = None
 

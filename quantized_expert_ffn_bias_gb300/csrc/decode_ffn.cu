@@ -152,27 +152,8 @@ __device__ __forceinline__ float f16_bits_to_float(uint32_t b) {
   return __half2float(__ushort_as_half((unsigned short)b));
 }
 
-// The packed dequant-dot of one 32-bit word of int4 codes (PTX text): codes at
-// mantissa positions, minus the magic pair %M, times four activation pairs.
-#define COLI_WORD4(Q, X01, X23, X45, X67, M, FIRST)                       \
-  "shr.b32 v, " Q ", 12;\n\t"                                             \
-  "lop3.b32 a0, " Q ", 0x0000000F, 0x4B000000, 0xEA;\n\t"                 \
-  "lop3.b32 a1, " Q ", 0x000000F0, 0x4B000000, 0xEA;\n\t"                 \
-  "lop3.b32 a2, " Q ", 0x00000F00, 0x4B000000, 0xEA;\n\t"                 \
-  "lop3.b32 a3, " Q ", 0x0000F000, 0x4B000000, 0xEA;\n\t"                 \
-  "lop3.b32 a4, " Q ", 0x000F0000, 0x4B000000, 0xEA;\n\t"                 \
-  "lop3.b32 a5, v, 0x00000F00, 0x4B000000, 0xEA;\n\t"                     \
-  "lop3.b32 a6, v, 0x0000F000, 0x4B000000, 0xEA;\n\t"                     \
-  "lop3.b32 a7, v, 0x000F0000, 0x4B000000, 0xEA;\n\t"                     \
-  "mov.b64 p0, {a0, a1};\n\tmov.b64 p1, {a2, a3};\n\t"                    \
-  "mov.b64 p2, {a4, a5};\n\tmov.b64 p3, {a6, a7};\n\t"                    \
-  "sub.rn.f32x2 p0, p0, " M ";\n\tsub.rn.f32x2 p1, p1, " M ";\n\t"        \
-  "sub.rn.f32x2 p2, p2, " M ";\n\tsub.rn.f32x2 p3, p3, " M ";\n\t"        \
-  FIRST                                                                   \
-  "fma.rn.f32x2 %0, p1, " X23 ", %0;\n\t"                                 \
-  "fma.rn.f32x2 %0, p2, " X45 ", %0;\n\t"                                 \
-  "fma.rn.f32x2 %0, p3, " X67 ", %0;\n\t"
-
+// The packed dequant-dot of one 32-bit word of int8 codes (PTX text): codes at
+// mantissa positions, minus the magic pair %M, times two activation pairs.
 #define COLI_WORD8(Q, X01, X23, M, FIRST)                                 \
   "shr.b32 v, " Q ", 16;\n\t"                                             \
   "lop3.b32 a0, " Q ", 0x000000FF, 0x4B000000, 0xEA;\n\t"                 \
@@ -183,46 +164,6 @@ __device__ __forceinline__ float f16_bits_to_float(uint32_t b) {
   "sub.rn.f32x2 p0, p0, " M ";\n\tsub.rn.f32x2 p1, p1, " M ";\n\t"        \
   FIRST                                                                   \
   "fma.rn.f32x2 %0, p1, " X23 ", %0;\n\t"
-
-// One row slice: 32 int4 codes (a 16-byte piece) against the lane's 32
-// pre-scaled activations (16 pairs), as a packed fp32 pair.  m2 = (2^23, 2^23).
-__device__ __forceinline__ uint64_t dot_row_int4(uint4 w, const ulonglong2 (&x)[8], uint64_t m2) {
-  uint64_t acc;
-  asm("{\n\t"
-      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
-      ".reg .b64 p0, p1, p2, p3;\n\t"
-      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "mul.rn.f32x2 %0, p0, %3;\n\t")
-      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
-      "}"
-      : "=l"(acc)
-      : "r"(w.x), "r"(w.y), "l"(x[0].x), "l"(x[0].y), "l"(x[1].x), "l"(x[1].y), "l"(x[2].x), "l"(x[2].y),
-        "l"(x[3].x), "l"(x[3].y), "l"(m2));
-#ifdef COLI_SPLIT_CHAIN
-  // words 2..3 in a second, independent chain (halves the dependent FMA chain)
-  uint64_t acc2;
-  asm("{\n\t"
-      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
-      ".reg .b64 p0, p1, p2, p3;\n\t"
-      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "mul.rn.f32x2 %0, p0, %3;\n\t")
-      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
-      "}"
-      : "=l"(acc2)
-      : "r"(w.z), "r"(w.w), "l"(x[4].x), "l"(x[4].y), "l"(x[5].x), "l"(x[5].y), "l"(x[6].x), "l"(x[6].y),
-        "l"(x[7].x), "l"(x[7].y), "l"(m2));
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(acc2));
-#else
-  asm("{\n\t"
-      ".reg .b32 v, a0, a1, a2, a3, a4, a5, a6, a7;\n\t"
-      ".reg .b64 p0, p1, p2, p3;\n\t"
-      COLI_WORD4("%1", "%3", "%4", "%5", "%6", "%11", "fma.rn.f32x2 %0, p0, %3, %0;\n\t")
-      COLI_WORD4("%2", "%7", "%8", "%9", "%10", "%11", "fma.rn.f32x2 %0, p0, %7, %0;\n\t")
-      "}"
-      : "+l"(acc)
-      : "r"(w.z), "r"(w.w), "l"(x[4].x), "l"(x[4].y), "l"(x[5].x), "l"(x[5].y), "l"(x[6].x), "l"(x[6].y),
-        "l"(x[7].x), "l"(x[7].y), "l"(m2));
-#endif
-  return acc;
-}
 
 // One row slice of 16 int8 codes against 16 pre-scaled activations (8 pairs).
 __device__ __forceinline__ uint64_t dot_row_int8(uint4 w, const ulonglong2 (&x)[8], uint64_t m2) {
@@ -240,7 +181,6 @@ __device__ __forceinline__ uint64_t dot_row_int8(uint4 w, const ulonglong2 (&x)[
         "l"(x[2].y), "l"(x[3].x), "l"(x[3].y), "l"(m2));
   return acc;
 }
-#undef COLI_WORD4
 #undef COLI_WORD8
 
 // One row slice of 32 int4 codes against the lane's fixed-point activations:
@@ -523,7 +463,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
           for (int r = 0; r < kRows; ++r) {
             const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
             const float2 sz = I4 ? tab[r * kGroupsPerStage + g] : tab[r];
-            const uint64_t d2 = I4 ? dot_row_int4(w, xq, m2) : dot_row_int8(w, xq, m2);
+            const uint64_t d2 = dot_row_int8(w, xq, m2);
             acc[t][r] = fmaf(sz.x, pair_sum(d2), fmaf(-sz.y, xsum, acc[t][r]));
           }
         }

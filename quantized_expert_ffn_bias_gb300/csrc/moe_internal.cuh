@@ -125,7 +125,6 @@ cudaError_t launch_route_decode(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
-cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_decode_down(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);

@@ -86,37 +86,6 @@ cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ dequant-GEMV input
-// xs[t][k] = x[t][k] * act_prescale(k), the activation of the dequant-GEMV kernels.
-__global__ void prep_xs_kernel(FwdArgs a) {
-  const size_t n = (size_t)a.T * a.d;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    const int k = (int)(i % a.d);
-    float v;
-    if (a.xtype == COLI_X_BF16) v = __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16);
-    else v = static_cast<const float*>(a.x)[i];
-    a.xs[i] = v * act_prescale(a.qtype, k);
-  }
-  const size_t nb = n / kXsumBlock;   // unscaled sums of x over blocks of 16 inputs
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < nb; i += (size_t)gridDim.x * blockDim.x) {
-    float sum = 0.f;
-    for (int j = 0; j < kXsumBlock; ++j) {
-      const size_t e = i * kXsumBlock + j;
-      sum += a.xtype == COLI_X_BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[e] << 16)
-                                    : static_cast<const float*>(a.x)[e];
-    }
-    a.xsum[i] = sum;
-  }
-}
-
-cudaError_t launch_prep_xs(const FwdArgs& a, cudaStream_t st) {
-  const size_t n = (size_t)a.T * a.d;
-  int blocks = (int)((n + 255) / 256);
-  if (blocks > 1024) blocks = 1024;
-  prep_xs_kernel<<<blocks, 256, 0, st>>>(a);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ int4 decode: h -> fixed point
 // The SwiGLU outputs of every grouped pair row (valid columns: F, or F_shared
 // for the shared expert's rows) in the fixed-point layout the int4 down kernel

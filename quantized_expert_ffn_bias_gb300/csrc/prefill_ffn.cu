@@ -34,12 +34,9 @@
 // issues the gate matrix and warp 22 the up matrix: the issuing thread sets the
 // pace, and two of them on different sub-partitions issue more MMAs); warps
 // 2..5 run the epilogue; warps 6..21 dequantise into a ring of TMEM A stages.
-// When every chunk has an even number of 128-row blocks, the CTAs launch as
-// clusters of two that run adjacent row blocks of the same chunk in lockstep
-// and share each stage's activation tiles by TMA multicast (see prefill_ffn_kernel).
+// Every CTA loads its own activation tiles with plain TMA loads.
 // All waits are bounded; a timeout sets the status word and every role stops.
 #include <algorithm>
-#include <atomic>
 
 #include "moe_internal.cuh"
 
@@ -53,10 +50,6 @@ constexpr int kPfDqWarps = 16;      // dequantising warps (four per TMEM sub-par
 constexpr int kPfThreads = (2 + kPfEpWarps + kPfDqWarps + 1) * 32;   // + second MMA issuer (gate/up)
 constexpr int kPfIssuer2Warp = 2 + kPfEpWarps + kPfDqWarps;
 constexpr int kPfAStagesMax = 8;    // deepest TMEM A ring (barrier arrays)
-#ifndef COLI_PREFILL_PAIR
-#define COLI_PREFILL_PAIR 1
-#endif
-constexpr bool kPfPair = COLI_PREFILL_PAIR != 0;   // clusters of 2 CTAs share activation tiles
 
 struct PfChunk { int slot, row0, ntok, pad; };
 struct PfTile { int chunk, mb, pad0, pad1; };
@@ -204,20 +197,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrive once on the mbarrier at this offset in every CTA of cta_mask when the
-// tensor-core operations issued so far by this thread have completed.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(cta_mask)
-               : "memory");
-}
-
-// All threads of both CTAs of a cluster (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -248,17 +227,6 @@ __device__ __forceinline__ void tma_load_2d_nohint(void* dst, const CUtensorMap*
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// 2D TMA load delivered to the same shared-memory offset, and completing on the
-// mbarrier at the same offset, in every CTA of the cluster named by cta_mask.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
 }
 
@@ -301,7 +269,6 @@ struct PfArgs {
   const CUtensorMap* wmaps;    // [(E+1)*3] raw-code maps (box: one stage of codes x 128 rows)
   __half* hout;                // gate/up: H [rows][Fmax] fp16 (column-permuted for int4)
   float* yout;                 // down: Y [rows][d] fp32
-  int pair;                    // 1: launched as clusters of 2 CTAs sharing the activation tiles
 };
 
 // TMEM: accumulators in columns [0, 2 * kPfN) (gate/up: gate and up of one
@@ -349,18 +316,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int n_tiles = *p.n_tiles;
   volatile int* abort_v = &abort_flag;
 
-  // Paired mode: the two CTAs of a cluster run the tiles 2q and 2q + 1, i.e. adjacent 128-row
-  // blocks of the same chunk, in lockstep.  Each loads half of every stage's activation atoms and
-  // multicasts them to both; a stage slot is refilled only when the MMA issuers of both CTAs
-  // have released it (their commits arrive on the slot's empty barrier in both CTAs).
-  const bool pair = p.pair != 0;
-  uint32_t crank = 0;
-  if (pair) asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
   if (threadIdx.x == 0) {
     constexpr int NI = GU ? 2 : 1;   // MMA-issuing threads (each commits)
     for (int s = 0; s < S; ++s) {
       mbar_init(&tma_full[s], 1);
-      mbar_init(&tma_empty[s], pair ? 2 * NI : NI);
+      mbar_init(&tma_empty[s], NI);
     }
     for (int s = 0; s < L::kAStages; ++s) {
       mbar_init(&a_full[s], kPfDqWarps);
@@ -381,7 +341,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (pair) cluster_sync_all();   // both CTAs' barriers are initialised before any multicast
   const uint32_t tmem = tmem_base;
 
   auto tile_info = [&](int t, int& slot, int& row0, int& ntok, int& mb, int& K) {
@@ -436,25 +395,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int m = 0; m < L::kMats; ++m)
             tma_load_2d_nohint(st + L::kBBytes + m * L::kRawBytes, p.wmaps + (size_t)slot * 3 + (GU ? m : 2),
                                kb * L::kRawRow, mb * kPfM, &tma_full[s]);
-          for (int at = 0; at < L::kAtoms; ++at) {
-            if (pair && (at & 1) != (int)crank) continue;   // the peer CTA loads this atom for both
-            for (int b = 0; b < nbox; ++b) {
-              uint8_t* dst = st + at * L::kBAtomBytes + b * kPfBBox * 128;
-              if (pair)
-                tma_load_2d_mc(dst, &bmap, kb * L::kStageK + at * 64, row0 + b * kPfBBox, &tma_full[s], 0x3);
-              else
-                tma_load_2d_nohint(dst, &bmap, kb * L::kStageK + at * 64, row0 + b * kPfBBox, &tma_full[s]);
-            }
-          }
+          for (int at = 0; at < L::kAtoms; ++at)
+            for (int b = 0; b < nbox; ++b)
+              tma_load_2d_nohint(st + at * L::kBAtomBytes + b * kPfBBox * 128, &bmap, kb * L::kStageK + at * 64,
+                                 row0 + b * kPfBBox, &tma_full[s]);
         }
         if (!ok) { fail_wait(); break; }
       }
-      // drain: every issued stage must have landed before the CTA can exit; paired, the peer's
-      // releases of the last stages (remote arrivals on this CTA's barriers) must have landed too
+      // drain: every issued stage must have landed before the CTA can exit
       const int issued = it;
       for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_full[j % S], (j / S) & 1);
-      if (pair)
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_empty[j % S], (j / S) & 1);
     }
   } else if (warp == 1 || (GU && warp == kPfIssuer2Warp)) {
     // ---------------------------------------------------------------- MMA issuers (gate/up: gate | up)
@@ -493,8 +443,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             } else {
               umma_k128(dacc, A + sub * (L::kStageK / 2), bd, idesc, kbf, (uint32_t)(L::kBAtomBytes >> 4));
             }
-            if (pair) umma_commit_mc(&tma_empty[s], 0x3);
-            else umma_commit(&tma_empty[s]);
+            umma_commit(&tma_empty[s]);
           }
           umma_commit(&a_empty[as]);
         }
@@ -691,7 +640,6 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
-  if (pair) cluster_sync_all();   // neither CTA leaves while its peer may still signal it
 }
 
 // ------------------------------------------------------------------ host side
@@ -705,47 +653,7 @@ static cudaError_t launch_pf(const FwdArgs& a, const PfArgs& p, const CUtensorMa
   auto kern = prefill_ffn_kernel<QT, GU>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  // Clusters of two CTAs on adjacent row blocks of a chunk share its activation tiles; this needs
-  // an even number of row blocks per chunk (then tiles 2q and 2q + 1 belong to the same chunk)
-  const bool even_blocks = GU ? ((a.F / kPfM) % 2 == 0 && (!a.has_shared || (a.Fs / kPfM) % 2 == 0))
-                              : ((a.d / kPfM) % 2 == 0);
-  static_assert(L::kAtoms % 2 == 0, "paired CTAs split the activation atoms of a stage");
-  if (kPfPair && even_blocks && num_sms >= 2) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(num_sms & ~1));
-    cfg.blockDim = dim3(kPfThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static std::atomic<int> cached{0};   // co-resident clusters of this kernel (one device per process)
-    int max_clusters = cached.load(std::memory_order_relaxed);
-    if (max_clusters == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        n = -1;
-      }
-      cached.store(n, std::memory_order_relaxed);
-      max_clusters = n;
-    }
-    if (max_clusters > 0) {
-      cfg.gridDim = dim3((unsigned)(2 * std::min(max_clusters, num_sms / 2)));
-      PfArgs q = p;
-      q.pair = 1;
-      e = cudaLaunchKernelEx(&cfg, kern, a, q, bmap);
-      if (e != cudaSuccess) return e;
-      return cudaGetLastError();
-    }
-  }
-  PfArgs q = p;
-  q.pair = 0;
-  kern<<<num_sms, kPfThreads, smem, st>>>(a, q, bmap);
+  kern<<<num_sms, kPfThreads, smem, st>>>(a, p, bmap);
   return cudaGetLastError();
 }
 
@@ -768,7 +676,7 @@ cudaError_t launch_plan_tiles(const FwdArgs& a, void* chunks, void* gu_tiles, vo
 cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
                                   const CUtensorMap* wmaps, const CUtensorMap& xmap, __half* hout, cudaStream_t st,
                                   int num_sms) {
-  PfArgs p{static_cast<const PfChunk*>(chunks), static_cast<const PfTile*>(tiles), n_tiles, wmaps, hout, nullptr, 0};
+  PfArgs p{static_cast<const PfChunk*>(chunks), static_cast<const PfTile*>(tiles), n_tiles, wmaps, hout, nullptr};
   return a.qtype == COLI_Q_INT4_G128 ? launch_pf<COLI_Q_INT4_G128, true>(a, p, xmap, st, num_sms)
                                      : launch_pf<COLI_Q_INT8_PC, true>(a, p, xmap, st, num_sms);
 }
@@ -776,7 +684,7 @@ cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const vo
 cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
                                 const CUtensorMap* wmaps, const CUtensorMap& hmap, float* yout, cudaStream_t st,
                                 int num_sms) {
-  PfArgs p{static_cast<const PfChunk*>(chunks), static_cast<const PfTile*>(tiles), n_tiles, wmaps, nullptr, yout, 0};
+  PfArgs p{static_cast<const PfChunk*>(chunks), static_cast<const PfTile*>(tiles), n_tiles, wmaps, nullptr, yout};
   return a.qtype == COLI_Q_INT4_G128 ? launch_pf<COLI_Q_INT4_G128, false>(a, p, hmap, st, num_sms)
                                      : launch_pf<COLI_Q_INT8_PC, false>(a, p, hmap, st, num_sms);
 }
