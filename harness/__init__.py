@@ -213,7 +213,7 @@ class Layer:
 
 
 def gen_bias(seed: int, layer: int, kind: str, E: int) -> np.ndarray:
-    """Router bias recipes: zero, uniform(a), normal(var), zipf(alpha, s), spike(e, value)."""
+    """Router bias recipes: zero, uniform(a), normal(std), zipf(alpha, s), spike(e, value)."""
     name, *args = kind.split(":")
     k = key(seed, _TAG_BIAS, layer)
     if name == "zero":
@@ -221,8 +221,8 @@ def gen_bias(seed: int, layer: int, kind: str, E: int) -> np.ndarray:
     if name == "uniform":
         a = float(args[0])
         return uniform(k, E, -a, a)
-    if name == "normal":          # N(0, var): std = sqrt(var)
-        return normal(k, E, 0.0, float(args[0]) ** 0.5)
+    if name == "normal":          # N(0, std^2): the argument is the standard deviation
+        return normal(k, E, 0.0, float(args[0]))
     if name == "zipf":            # b_e = -alpha * s * ln(rank_e), rank a seeded permutation of 1..E
         alpha, s = float(args[0]), float(args[1])
         rank = permutation(key(seed, _TAG_PERM, layer), E).astype(np.float64) + 1.0
