@@ -1,12 +1,18 @@
 """Benchmark of the quantized sparse MoE layer forward on one GB300 (or N independent replicas).
 
-Default workload: the GLM-5.2-class decode layer (d=7168, d_ff=2048, 256 experts,
-top-8, int4 group-128 weights, routed scale 2.5, bias 0, bf16 x), T=1 token per
-step, with the T=4 variant reported alongside.  A step is one full layer
-forward (router, grouping, gate/up + SwiGLU, down, combine) on a fresh x, so
-routing differs every step; the 5.9 GB expert set is far larger than L2.
+Default run (``--workload all``): the five GLM-5.2-class workloads, each on its own
+resident expert set, with the decode layer at T=1 as the headline of the JSON
+line and the others under ``variants``:
+  decode T=1 / T=4  d=7168, d_ff=2048, 256 experts, top-8, int4 group-128, routed scale 2.5, bias 0
+  mtp_verify T=3    the same plus a shared int4 expert, router bias N(0, std 0.5)
+  prefill T=2048    the same plus a shared expert, Zipf-skewed router bias
+  stacked T=256     six layers (int4 / int8 alternating) with RMSNorm and residual, 51.4 GB resident
+A step is one full forward (router, grouping, gate/up + SwiGLU, down, combine; for the stacked workload
+the whole stack) on a fresh x, so routing differs every step; every expert set is far larger than L2.
+Each entry carries its own roofline, end-to-end figure, CPU baseline (the oracle), clock record and
+routing statistics (near-tie tokens, unique experts per step).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|mtp_verify|prefill|stacked]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores (CPU baseline arm)
 
 Prints one JSON line (rank 0).
@@ -151,9 +157,10 @@ def workload_config(w, T: int, world: int) -> dict:
                   % (expert_set_bytes(w) / 1e9)}
 
 
-def unique_expert_bytes(dl, T) -> tuple[int, int]:
+def unique_expert_bytes(dl, T, idx=None) -> tuple[int, int]:
     """(gate+up bytes, down bytes) streamed by the last forward: unique routed experts + shared."""
-    idx = dl.routing(T)[0]
+    if idx is None:
+        idx = dl.routing(T)[0]
     U = len(np.unique(idx))
     L = dl.layer
     gu = L.experts.gate.nbytes // L.E + L.experts.up.nbytes // L.E
@@ -175,8 +182,9 @@ DECODE_GATEUP_T1_TRAFFIC = 122_086_656 + 3_052_288
 # summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,090,944 B read + 17,734,656 B
 # written).  Both the expert bytes and the gathered activations grow with E and T by the same factor 4
 # (the one shared expert does not: 15 MB of the 4.3 GB); the full-size launch is too large to capture
-# with more than a one-pass metric.  None whenever that kernel changes.
-PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_067_090_944 + 17_734_656)
+# with more than a one-pass metric.  None whenever that kernel changes (it has since that capture: the
+# CTAs no longer run in pairs that share activation tiles).
+PREFILL_GATEUP_T2048_TRAFFIC = None
 
 
 def max_over_ranks(v: float, device=None) -> float:
@@ -203,176 +211,13 @@ def expert_flops(layer, T: int) -> tuple[float, float]:
     return 2.0 * 2 * layer.d * pairs_f, 2.0 * layer.d * pairs_f
 
 
-def bench_native(args, rank: int, world: int):
+def _timed_steps(run_step, xs, W: int, K: int, dev, world: int, stream):
+    """W untimed warm-up steps, then K steps between CUDA events on the launching stream (synchronised and,
+    with replicas, behind a barrier on both sides) while nvidia-smi samples the clocks.  Returns
+    (device ms for the K steps, clock summary)."""
     import torch
-    import quantized_expert_ffn_bias_gb300 as coli
-    from harness.device import DeviceLayer, to_dev
-
-    coli.build()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w, T_main, Ts = workload_setup(args.workload, args.experts, args.tokens)
-    t0 = time.time()
-    layer = w.layer(0)
-    dl = DeviceLayer(layer, max(Ts), device=dev)
-    gen_s = time.time() - t0
-    stream = torch.cuda.current_stream(dev)
-    K, W = args.steps, args.warmup
-    pk = peaks()
-    results = {}
-    for T in Ts:
-        nx = K + W
-        xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(nx)]
-        out = torch.empty((T, layer.d), dtype=torch.float32, device=dev)
-        for i in range(W):
-            dl.forward(xs[i], out=out)
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
-        # ---- timed region (device time, CUDA events on the launching stream)
-        with ClockSampler(dev.index) as clk:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            e0.record(stream)
-            for i in range(K):
-                dl.forward(xs[W + i], out=out)
-            e1.record(stream)
-            torch.cuda.synchronize(dev)
-            if world > 1:
-                torch.distributed.barrier()
-        ms = e0.elapsed_time(e1)
-        launches = dl.plan.last_launch_count()
-        # ---- per-kernel times (same steps again, kernel-boundary events recorded by the library)
-        dl.plan.profile_begin(K)
-        for i in range(K):
-            dl.forward(xs[W + i], out=out)
-        torch.cuda.synchronize(dev)
-        kt = dl.plan.profile_end()
-        # algorithmic bytes of the gate/up and down kernels for these K steps
-        gub, dnb = 0, 0
-        for i in range(K):
-            dl.forward(xs[W + i], out=out)
-            torch.cuda.synchronize(dev)
-            a, b = unique_expert_bytes(dl, T)
-            gub += a
-            dnb += b
-        # ---- end to end through the public API with host buffers (pinned), copies inside the timed region
-        xh = [torch.empty_like(xs[0], device="cpu").pin_memory() for _ in range(K)]
-        for i in range(K):
-            xh[i].copy_(xs[W + i].cpu())
-        oh = torch.empty((K, T, layer.d), dtype=torch.float32).pin_memory()
-        xd = torch.empty_like(xs[0])
-        torch.cuda.synchronize(dev)
-        t_e2e0 = time.perf_counter()
-        for i in range(K):
-            xd.copy_(xh[i], non_blocking=True)
-            dl.forward(xd, out=out)
-            oh[i].copy_(out, non_blocking=True)
-        torch.cuda.synchronize(dev)
-        e2e_s = time.perf_counter() - t_e2e0
-        results[T] = dict(ms=ms, kt=kt, launches=launches, gub=gub, dnb=dnb, clocks=clk.summary(), e2e_s=e2e_s,
-                          h2d=xh[0].numel() * xh[0].element_size(), d2h=T * layer.d * 4)
-        del xs
-    def mx(v):
-        return max_over_ranks(v, dev)
-
-    lines = {}
-    for T, r in results.items():
-        ms_tot = mx(r["ms"])
-        e2e_tot = mx(r["e2e_s"])
-        kt = r["kt"]
-        gu_ms, gu_n = kt.get("expert_gate_up", (0.0, 0))
-        dn_ms, dn_n = kt.get("expert_down", (0.0, 0))
-        step_kernel_ms = sum(v[0] for v in kt.values()) / K
-        achieved = (r["gub"] / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
-        achieved_d = (r["dnb"] / dn_n) / (dn_ms / dn_n * 1e-3) / 1e9 if dn_n else None
-        layer_gbs = (r["gub"] + r["dnb"]) / K / (ms_tot / K * 1e-3) / 1e9
-        if args.workload == "prefill":
-            # dense contraction: the tensor-core grouped GEMMs against the bf16/fp16 tensor peak
-            # (sustained figure: the kernels run inside multi-millisecond steps)
-            gfl, dfl = expert_flops(dl.layer, T)
-            tg_ms, tg_n = kt.get("tc_gate_up", (0.0, 0))
-            td_ms, td_n = kt.get("tc_down", (0.0, 0))
-            pk_t = pk["bf16_tflops_sustained"]
-            ach = gfl / (tg_ms / tg_n * 1e-3) / 1e12 if tg_n else None
-            ach_d = dfl / (td_ms / td_n * 1e-3) / 1e12 if td_n else None
-            layer_tf = (gfl + dfl) / (ms_tot / K * 1e-3) / 1e12
-            roof = {"bound": "tensor", "kernel": "tc_gate_up", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
-                    "frac": (ach / pk_t) if ach else None,
-                    "traffic": PREFILL_GATEUP_T2048_TRAFFIC if (T == 2048 and not args.experts) else None,
-                    "peak_source": pk["source"] + " (bf16 dense, sustained; fp16 runs at the same rate)",
-                    "algorithmic_flops_per_launch": gfl, "down_kernel_achieved_tflops": ach_d,
-                    "layer_tflops": layer_tf, "layer_frac_of_burst_peak": layer_tf / pk["bf16_tflops"]}
-        else:
-            roof = {"bound": "hbm", "kernel": "expert_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
-                    "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
-                    "traffic": DECODE_GATEUP_T1_TRAFFIC if (T == 1 and args.workload == "decode"
-                                                            and not args.experts) else None,
-                    "peak_source": pk["source"],
-                    "algorithmic_bytes_per_launch": r["gub"] / max(gu_n, 1),
-                    "down_kernel_achieved_gbs": achieved_d}
-        lines[T] = {
-            "metric": METRIC,
-            "value": replica_tokens_per_s(world, K, T, ms_tot),
-            "unit": "tokens/s",
-            "ms_per_step": ms_tot / K,
-            "hbm_gbs_layer": layer_gbs,
-            "hbm_frac_layer": layer_gbs / pk["hbm_gbs"],
-            "roofline": roof,
-            "kernel_ms_per_step": {k: v[0] / v[1] for k, v in kt.items()},
-            "kernel_share": {k: v[0] / max(sum(x[0] for x in kt.values()), 1e-12) for k, v in kt.items()},
-            "kernel_sum_ms_per_step": step_kernel_ms,
-            "e2e": {"value": world * K * T / e2e_tot, "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"]},
-            "gpu_launches": K * r["launches"],
-            "clocks": r["clocks"],
-        }
-    return w, T_main, Ts, lines, gen_s
-
-
-def bench_stacked(args, world: int):
-    """Six stacked layers h <- h + MoE(bf16(RMSNorm(h))) per step (T=256, alternating int4 / int8 experts,
-    51.4 GB resident); a step is the whole stack on a fresh input."""
-    import torch
-    import quantized_expert_ffn_bias_gb300 as coli
-    from harness.device import DeviceLayer, to_dev
-
-    coli.build()
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w, T, _ = workload_setup("stacked", args.experts, args.tokens)
-    t0 = time.time()
-    dls, expert_bytes = [], []
-    for l in range(w.n_layers):
-        layer = w.layer(l)
-        dl = DeviceLayer(layer, T, device=dev)
-        per_expert = (layer.experts.gate.nbytes + layer.experts.up.nbytes + layer.experts.down.nbytes) // layer.E
-        expert_bytes.append((per_expert, layer.qtype))
-        dl.experts.bank = None          # keep only the device copies
-        dl.layer = None
-        dls.append((dl, layer.E, layer.k))
-        del layer
-    gen_s = time.time() - t0
-    stream = torch.cuda.current_stream(dev)
-    eps = w.rmsnorm_eps
-    K, W = args.steps, args.warmup
-    xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(K + W)]
-    h = torch.empty((T, w.d), dtype=torch.float32, device=dev)
-    h2 = torch.empty_like(h)
-    n = torch.empty((T, w.d), dtype=torch.int16, device=dev)
-
-    def step(x):
-        nonlocal h, h2
-        h.copy_(x.view(torch.bfloat16).float())
-        for dl, _, _ in dls:
-            coli.colibri_moe_rmsnorm_bf16(h, T, w.d, eps, n, stream)
-            dl.forward(n, out=h2, residual=h)
-            h, h2 = h2, h
-        return h
-
     for i in range(W):
-        step(xs[i])
+        run_step(xs[i])
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -382,26 +227,192 @@ def bench_stacked(args, world: int):
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for i in range(K):
-            step(xs[W + i])
+            run_step(xs[W + i])
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
-    ms = max_over_ranks(e0.elapsed_time(e1), dev)
-    # per-kernel times and unique-expert bytes per layer
-    for dl, _, _ in dls:
-        dl.plan.profile_begin(K)
-    uniq = [0] * len(dls)
+    return e0.elapsed_time(e1), clk.summary()
+
+
+def _e2e_steps(run_step, xs_dev, K: int, W: int, out_shape, dev):
+    """The same K steps through the public API with host buffers: every step copies its x from pinned host
+    memory to the device and its output back to pinned host memory inside the timed region.  Returns
+    (seconds, H2D bytes per step, D2H bytes per step)."""
+    import torch
+    xh = [torch.empty_like(xs_dev[0], device="cpu").pin_memory() for _ in range(K)]
     for i in range(K):
-        x = xs[W + i]
+        xh[i].copy_(xs_dev[W + i].cpu())
+    oh = torch.empty((K,) + tuple(out_shape), dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(xs_dev[0])
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(K):
+        xd.copy_(xh[i], non_blocking=True)
+        out = run_step(xd)
+        oh[i].copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    return time.perf_counter() - t0, xh[0].numel() * xh[0].element_size(), oh[0].numel() * 4
+
+
+def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
+    """One MoE layer workload (decode, mtp_verify or prefill): every T of the workload is timed on the same
+    resident expert set.  Returns ({T: line fragment}, cpu_baseline or None, host generation seconds)."""
+    import torch
+    from harness.device import DeviceLayer, to_dev
+
+    w, _, Ts = workload_setup(name, args.experts, args.tokens)
+    t0 = time.time()
+    layer = w.layer(0)
+    dl = DeviceLayer(layer, max(Ts), device=dev)
+    gen_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+    pk = peaks()
+    frags = {}
+    for T in Ts:
+        xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(K + W)]
+        out = torch.empty((T, layer.d), dtype=torch.float32, device=dev)
+
+        def step(x):
+            return dl.forward(x, out=out)
+
+        ms, clocks = _timed_steps(step, xs, W, K, dev, world, stream)
+        launches = dl.plan.last_launch_count()
+        # per-kernel times: the same steps again, kernel-boundary events recorded by the library
+        dl.plan.profile_begin(K)
+        for i in range(K):
+            step(xs[W + i])
+        torch.cuda.synchronize(dev)
+        kt = dl.plan.profile_end()
+        # algorithmic bytes and routing statistics of these K steps (each step re-run and read back)
+        gub = dnb = 0
+        near = uniq = 0
+        for i in range(K):
+            step(xs[W + i])
+            torch.cuda.synchronize(dev)
+            idx, _, nt = dl.routing(T)[:3]
+            a, b = unique_expert_bytes(dl, T, idx)
+            gub += a
+            dnb += b
+            near += int(nt.sum())
+            uniq += len(np.unique(idx))
+        e2e_s, h2d, d2h = _e2e_steps(step, xs, K, W, (T, layer.d), dev)
+        ms_tot, e2e_tot = max_over_ranks(ms, dev), max_over_ranks(e2e_s, dev)
+        gu_ms, gu_n = kt.get("expert_gate_up", (0.0, 0))
+        dn_ms, dn_n = kt.get("expert_down", (0.0, 0))
+        layer_gbs = (gub + dnb) / K / (ms_tot / K * 1e-3) / 1e9
+        if T > 8:
+            # dense contraction: the tensor-core grouped GEMMs against the bf16/fp16 tensor peak
+            gfl, dfl = expert_flops(layer, T)
+            tg_ms, tg_n = kt.get("tc_gate_up", (0.0, 0))
+            td_ms, td_n = kt.get("tc_down", (0.0, 0))
+            pk_t, pk_b = pk["bf16_tflops_sustained"], pk["bf16_tflops"]
+            ach = gfl / (tg_ms / tg_n * 1e-3) / 1e12 if tg_n else None
+            ach_d = dfl / (td_ms / td_n * 1e-3) / 1e12 if td_n else None
+            layer_tf = (gfl + dfl) / (ms_tot / K * 1e-3) / 1e12
+            roof = {"bound": "tensor", "kernel": "tc_gate_up", "achieved": ach, "peak": pk_t, "unit": "TFLOP/s",
+                    "frac": (ach / pk_t) if ach else None, "frac_of_burst_peak": (ach / pk_b) if ach else None,
+                    "traffic": PREFILL_GATEUP_T2048_TRAFFIC if (T == 2048 and not args.experts) else None,
+                    "peak_source": pk["source"] + " bf16 dense, sustained (fp16 operands run at the bf16 rate)",
+                    "algorithmic_flops_per_launch": gfl, "down_kernel_achieved_tflops": ach_d,
+                    "layer_tflops": layer_tf, "layer_frac_of_sustained_peak": layer_tf / pk_t,
+                    "layer_frac_of_burst_peak": layer_tf / pk_b}
+        else:
+            achieved = (gub / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
+            achieved_d = (dnb / dn_n) / (dn_ms / dn_n * 1e-3) / 1e9 if dn_n else None
+            roof = {"bound": "hbm", "kernel": "expert_gate_up", "achieved": achieved, "peak": pk["hbm_gbs"],
+                    "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                    "traffic": DECODE_GATEUP_T1_TRAFFIC if (T == 1 and name == "decode" and not args.experts)
+                    else None,
+                    "peak_source": pk["source"], "algorithmic_bytes_per_launch": gub / max(gu_n, 1),
+                    "down_kernel_achieved_gbs": achieved_d}
+        frags[T] = {
+            "value": replica_tokens_per_s(world, K, T, ms_tot),
+            "unit": "tokens/s",
+            "ms_per_step": ms_tot / K,
+            "hbm_gbs_layer": layer_gbs,
+            "hbm_frac_layer": layer_gbs / pk["hbm_gbs"],
+            "roofline": roof,
+            "kernel_ms_per_step": {k: v[0] / v[1] for k, v in kt.items()},
+            "kernel_share": {k: v[0] / max(sum(x[0] for x in kt.values()), 1e-12) for k, v in kt.items()},
+            "e2e": {"value": world * K * T / e2e_tot, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": K * launches,
+            "clocks": clocks,
+            "routing": {"tokens": K * T, "near_tie_tokens": near, "unique_experts_per_step": uniq / K,
+                        "near_tie_rule": "k-th minus (k+1)-th selection score < 1e-5, flagged by the GPU router"},
+            "config": workload_config(w, T, world),
+        }
+        del xs
+    cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
+    dl.close()
+    del dl, layer
+    torch.cuda.empty_cache()
+    return frags, cpu, gen_s
+
+
+def bench_stacked(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
+    """Six stacked layers h <- h + MoE(bf16(RMSNorm(h))) per step (T=256, alternating int4 / int8 experts,
+    51.4 GB resident); a step is the whole stack on a fresh input."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+
+    w, T, _ = workload_setup("stacked", args.experts, args.tokens)
+    t0 = time.time()
+    dls, expert_bytes, cpu_rates, cpu_samples = [], [], {}, []
+    cores = None
+    for l in range(w.n_layers):
+        layer = w.layer(l)
+        dl = DeviceLayer(layer, T, device=dev)
+        expert_bytes.append(layer.experts.bytes_per_expert)
+        if want_cpu and layer.qtype not in cpu_rates:
+            # the oracle's rate on one layer of each quantisation type (the stack's cost is three of each)
+            r = cpu_baseline(w, layer, T, cpu_budget_s / 2)
+            cpu_rates[layer.qtype] = r["value"]
+            cores = r["cores"]
+            cpu_samples.append(f"layer {l} ({'int4' if layer.qtype == H.Q_INT4_G128 else 'int8'}): {r['sample']}")
+        dl.experts.bank = None          # keep only the device copies
+        dl.layer = None
+        dls.append((dl, layer.E, layer.k))
+        del layer
+    gen_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+    eps = w.rmsnorm_eps
+    K, W = args.steps, args.warmup
+    xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(K + W)]
+    hb = [torch.empty((T, w.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    n = torch.empty((T, w.d), dtype=torch.int16, device=dev)
+
+    def step(x, routing=None):
+        h, h2 = hb
         h.copy_(x.view(torch.bfloat16).float())
         for li, (dl, E, k) in enumerate(dls):
             coli.colibri_moe_rmsnorm_bf16(h, T, w.d, eps, n, stream)
             dl.forward(n, out=h2, residual=h)
-            idx = torch.empty((T, k), dtype=torch.int32, device=dev)
-            dl.plan.debug_routing(dl.ws, T, idx, stream=stream)
-            uniq[li] += int(torch.unique(idx).numel())
+            if routing is not None:
+                routing(li, dl, k)
             h, h2 = h2, h
+        return h
+
+    ms, clocks = _timed_steps(step, xs, W, K, dev, world, stream)
+    ms = max_over_ranks(ms, dev)
+    # per-kernel times, unique experts and near-ties per layer (the same steps again)
+    for dl, _, _ in dls:
+        dl.plan.profile_begin(K)
+    uniq = [0] * len(dls)
+    near = [0]
+
+    def rec(li, dl, k):
+        idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+        nt = torch.empty(T, dtype=torch.int32, device=dev)
+        dl.plan.debug_routing(dl.ws, T, idx, None, nt, stream=stream)
+        uniq[li] += int(torch.unique(idx).numel())
+        near[0] += int(nt.sum().item())
+
+    for i in range(K):
+        step(xs[W + i], routing=rec)
     torch.cuda.synchronize(dev)
     kt_all = {}
     for dl, _, _ in dls:
@@ -409,67 +420,100 @@ def bench_stacked(args, world: int):
             a = kt_all.setdefault(kname, [0.0, 0])
             a[0] += tms
             a[1] += n_l
-    alg_bytes = sum(uniq[li] * expert_bytes[li][0] for li in range(len(dls))) / K   # per step
+    alg_bytes = sum(uniq[li] * expert_bytes[li] for li in range(len(dls))) / K   # per step
     gu_ms, gu_n = kt_all.get("tc_gate_up", (0.0, 0))
-    gu_bytes = sum(uniq[li] * expert_bytes[li][0] * 2 // 3 for li in range(len(dls))) / K
+    gu_bytes = sum(uniq[li] * expert_bytes[li] * 2 // 3 for li in range(len(dls))) / K
     pk = peaks()
     ach = (gu_bytes * K / gu_n) / (gu_ms / gu_n * 1e-3) / 1e9 if gu_n else None
     step_gbs = alg_bytes / (ms / K * 1e-3) / 1e9
-    # end to end through the public API: x (bf16) from pinned host memory, h back to pinned host memory
-    xh = [torch.empty_like(xs[0], device="cpu").pin_memory() for _ in range(K)]
-    for i in range(K):
-        xh[i].copy_(xs[W + i].cpu())
-    oh = torch.empty((K, T, w.d), dtype=torch.float32).pin_memory()
-    xd = torch.empty_like(xs[0])
-    torch.cuda.synchronize(dev)
-    te = time.perf_counter()
-    for i in range(K):
-        xd.copy_(xh[i], non_blocking=True)
-        out = step(xd)
-        oh[i].copy_(out, non_blocking=True)
-    torch.cuda.synchronize(dev)
-    e2e_s = max_over_ranks(time.perf_counter() - te, dev)
+    e2e_s, h2d, d2h = _e2e_steps(step, xs, K, W, (T, w.d), dev)
+    e2e_s = max_over_ranks(e2e_s, dev)
+    cpu = None
+    if want_cpu and len(cpu_rates) == 2:
+        per_tok_s = sum(3.0 / r for r in cpu_rates.values())
+        cpu = {"value": 1.0 / per_tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "oracle rate of one int4 and one int8 layer, combined as 3 + 3 layers per token "
+                         "(RMSNorm is negligible); " + "; ".join(cpu_samples)}
     line = {
-        "metric": METRIC, "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
+        "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
         "ms_per_step": ms / K, "hbm_gbs_layer": step_gbs, "hbm_frac_layer": step_gbs / pk["hbm_gbs"],
         "roofline": {"bound": "hbm", "kernel": "tc_gate_up", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": (ach / pk["hbm_gbs"]) if ach else None, "traffic": None, "peak_source": pk["source"],
                      "algorithmic_bytes_per_launch": gu_bytes / len(dls)},
         "kernel_ms_per_step": {k2: v[0] / K for k2, v in kt_all.items()},
-        "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s",
-                "h2d_bytes_per_step": xh[0].numel() * xh[0].element_size(), "d2h_bytes_per_step": T * w.d * 4},
+        "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
         "gpu_launches": K * sum(dl.plan.last_launch_count() + 1 for dl, _, _ in dls),
-        "clocks": clk.summary(),
-        "n_gpus": world, "steps": K, "warmup": W, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int4/int8-weights, fp16 tensor-core operands, f32 accumulate",
-        "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
+        "clocks": clocks,
+        "routing": {"tokens": K * T * len(dls), "near_tie_tokens": near[0],
+                    "unique_experts_per_step_per_layer": [u / K for u in uniq]},
         "config": workload_config(w, T, world),
-        "host_generation_s": round(gen_s, 1),
-        "cpu_baseline": None,
+        "cpu_baseline": cpu,
     }
-    return line
+    for dl, _, _ in dls:
+        dl.close()
+    del dls, xs
+    torch.cuda.empty_cache()
+    return line, gen_s
 
 
-def cpu_baseline(w, T: int, budget_s: float = 12.0):
-    """The oracle as it stands on this host's cores, on a bounded sample of the workload's tokens."""
+def cpu_baseline(w, layer, T: int, budget_s: float):
+    """The oracle as it stands on this host's cores (OpenMP over tokens), on a bounded sample of the
+    workload's tokens: calls of `cores` tokens each until `budget_s` seconds have passed."""
     import oracle as O
-    layer = w.layer(0)
     orc = O.Oracle(layer)
     cores = O.default_threads()
     n_tok = max(1, cores)
     x = w.x(max(T, n_tok), 77)
+    toks = np.arange(n_tok, dtype=np.int32) % x.shape[0]
     t0 = time.perf_counter()
     done = 0
     while True:
-        orc.forward(x, tokens=np.arange(done % x.shape[0], done % x.shape[0] + 1, dtype=np.int32) if n_tok == 1
-                    else np.arange(n_tok, dtype=np.int32) % x.shape[0], nthreads=cores)
+        orc.forward(x, tokens=toks, nthreads=cores)
         done += n_tok
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
     return {"value": done / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{done} tokens of the {w.name} workload (d={w.d}, d_ff={w.F}, E={w.E}, k={w.k}), "
-                      f"{n_tok} tokens per call over {cores} threads, {dt:.1f} s"}, layer
+            "sample": f"{done} tokens of the {w.name} workload (d={w.d}, d_ff={w.F}, E={w.E}, k={w.k}"
+                      f"{', shared d_ff=%d' % w.F_shared if w.F_shared else ''}), {n_tok} tokens per call over "
+                      f"{cores} threads, {dt:.1f} s"}
+
+
+def reference_arm(args, world: int, rank: int):
+    """The oracle as it stands, timed on the host cores on the headline workload (decode, T=1)."""
+    if rank != 0:
+        return
+    name = "decode" if args.workload == "all" else args.workload
+    w, T_main, _ = workload_setup(name, args.experts, args.tokens)
+    import oracle as O
+    layer = w.layer(0)
+    orc = O.Oracle(layer)
+    cores = O.default_threads()
+    n_tok = max(1, min(cores, 16))
+    x = w.x(max(n_tok, T_main), 77)
+    toks = np.arange(n_tok, dtype=np.int32) % x.shape[0]
+    for _ in range(args.warmup):
+        orc.forward(x, tokens=toks[:1], nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.forward(x, tokens=toks, nthreads=cores)
+    dt = time.perf_counter() - t0
+    v = args.steps * n_tok / dt
+    sample = f"{n_tok} tokens per step of the {w.name} workload, {cores} threads"
+    # n_gpus: the launch's N (the oracle itself runs on the host cores, as cpu_baseline says)
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic",
+                      "config": workload_config(w, T_main, world),
+                      "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                       "sample": sample},
+                      "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+VARIANT_KEYS = ("value", "unit", "ms_per_step", "hbm_gbs_layer", "hbm_frac_layer", "roofline", "kernel_ms_per_step",
+                "e2e", "gpu_launches", "clocks", "routing", "config", "cpu_baseline")
 
 
 def main():
@@ -478,74 +522,63 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "mtp_verify", "prefill", "stacked"])
+    ap.add_argument("--workload", default="all", choices=["all", "decode", "mtp_verify", "prefill", "stacked"],
+                    help="all (default): decode T=1 as the headline with decode T=4, MTP verify, prefill and the "
+                         "stacked layers as variants; otherwise that workload alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--experts", type=int, default=0, help="override E (reduced case for profiler captures)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (reduced case for profiler captures)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    w, T_main, Ts = None, None, None
-
     if args.impl == "reference":
-        if rank != 0:
-            return
-        w, T_main, Ts = workload_setup(args.workload, args.experts, args.tokens)
-        import oracle as O
-        layer = w.layer(0)
-        orc = O.Oracle(layer)
-        cores = O.default_threads()
-        n_tok = max(1, min(cores, 16))
-        x = w.x(max(n_tok, T_main), 77)
-        toks = np.arange(n_tok, dtype=np.int32) % x.shape[0]
-        for _ in range(args.warmup):
-            orc.forward(x, tokens=toks[:1], nthreads=cores)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            orc.forward(x, tokens=toks, nthreads=cores)
-        dt = time.perf_counter() - t0
-        v = args.steps * n_tok / dt
-        sample = f"{n_tok} tokens per step of the {w.name} workload, {cores} threads"
-        # n_gpus: the launch's N (the oracle itself runs on the host cores, as cpu_baseline says)
-        print(json.dumps({"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                          "data": "synthetic",
-                          "config": workload_config(w, T_main, world),
-                          "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                           "sample": sample},
-                          "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        reference_arm(args, world, rank)
         return
 
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    coli.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
     if world > 1:
-        import torch
         import torch.distributed as dist
-        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         dist.init_process_group("nccl")
-    if args.workload == "stacked":
-        line = bench_stacked(args, world)
-        if rank == 0:
-            print(json.dumps(line))
-        return
-    w, T_main, Ts, lines, gen_s = bench_native(args, rank, world)
+    want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    names = ["decode", "mtp_verify", "prefill", "stacked"] if args.workload == "all" else [args.workload]
+    results, gen_total = [], 0.0
+    for name in names:
+        budget = 10.0 if name == names[0] else 6.0
+        if name == "stacked":
+            line, gen_s = bench_stacked(args, dev, world, want_cpu, budget)
+            ws, T_s, _ = workload_setup("stacked", args.experts, args.tokens)
+            results.append((f"stacked {ws.n_layers} layers T={T_s}", "stacked", None, line))
+        else:
+            frags, cpu, gen_s = bench_layer(name, args, dev, world, want_cpu, budget)
+            for i, (T, fr) in enumerate(frags.items()):
+                fr["cpu_baseline"] = cpu if i == 0 else None
+                results.append((f"{name} T={T}", name, T, fr))
+        gen_total += gen_s
     if rank != 0:
         return
-    line = dict(lines[T_main])
-    cpu = None
-    if not args.no_cpu_baseline:
-        cpu, _ = cpu_baseline(w, T_main)
+    head_label, head_name, head_T, head = results[0]
+    w = H.WORKLOADS[head_name]
+    line = {"metric": METRIC}
+    line.update({k: head[k] for k in VARIANT_KEYS if k in head})
+    if head_name == "stacked":
+        dtype = "int4/int8-weights, fp16 tensor-core operands, f32 accumulate"
+    elif head_T is not None and head_T > 8:
+        dtype = "int4-weights, fp16 tensor-core operands, f32 accumulate"
+    else:
+        dtype = "int4-weights, int32 dot products, f32 accumulate"
     line.update({
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "int4-weights/f32-accumulate" if w.qtypes[0] == 0 else "int8",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype,
         "data": "synthetic (seeded; GLM-5.2-class shapes, random-init quantised experts)",
-        "config": workload_config(w, T_main, world),
-        "host_generation_s": round(gen_s, 1),
-        "cpu_baseline": cpu,
+        "host_generation_s": round(gen_total, 1),
     })
-    line["variants"] = {f"T={T}": {k: lines[T][k] for k in ("value", "ms_per_step", "hbm_gbs_layer",
-                                                            "hbm_frac_layer", "roofline", "kernel_ms_per_step",
-                                                            "e2e", "gpu_launches")}
-                        for T in Ts if T != T_main}
+    line["variants"] = {}
+    for label, name, T, fr in results[1:]:
+        line["variants"][label] = {k: fr[k] for k in VARIANT_KEYS if k in fr}
     print(json.dumps(line))
 
 
