@@ -214,6 +214,30 @@ COLI_API coli_status colibri_moe_check_status(const coli_moe_plan_t* plan, const
                                      void* stream);
 
 /*
+ * Failure-path testing (no counterpart in the pages: it exercises the
+ * bounded waits and the expert-id check above).  Makes the following forward
+ * calls of this plan:
+ *   COLI_INJECT_WITHHOLD_STAGE  skip the TMA issue of one pipeline stage of the
+ *                               gate/up expert kernel (the first stage of warp 0
+ *                               of CTA 0 at decode, of CTA 0 at prefill), so
+ *                               that the roles waiting on it reach the wait
+ *                               limit, record COLI_DEV_WAIT_TIMEOUT, drain what
+ *                               they issued, free tensor memory and return;
+ *   COLI_INJECT_BAD_EXPERT_ID   replace the first chosen expert id of token 0
+ *                               by -1 before grouping, so that the grouping step
+ *                               records COLI_DEV_BAD_EXPERT_ID and leaves that
+ *                               pair out of the output.
+ * Nothing faults or hangs: every wait stays bounded.  wait_limit_ms > 0 sets
+ * the limit of every pipeline wait (default ~1000 ms); <= 0 restores it.
+ * flags = 0 turns injection off.  The outputs of an injected forward are not
+ * meaningful; the next forward without injection is a normal one.
+ * Errors: COLI_EINVAL (null plan or unknown flag bits).
+ */
+#define COLI_INJECT_WITHHOLD_STAGE 1
+#define COLI_INJECT_BAD_EXPERT_ID 2
+COLI_API coli_status colibri_moe_debug_inject(coli_moe_plan_t* plan, int flags, double wait_limit_ms);
+
+/*
  * Per-kernel timing (the per-stage share that a "--profile" run reports).
  * colibri_moe_profile_begin(plan, max_calls) makes the next forward calls
  * record a CUDA event before and after every kernel, on the launching stream,

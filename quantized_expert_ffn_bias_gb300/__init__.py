@@ -20,6 +20,7 @@ COLI_OK, COLI_EINVAL, COLI_EALIGN, COLI_EUNSUPPORTED, COLI_EWORKSPACE, COLI_ECUD
 COLI_Q_INT4_G128, COLI_Q_INT8_PC = 0, 1
 COLI_X_BF16, COLI_X_F32 = 0, 1
 COLI_DEV_BAD_EXPERT_ID, COLI_DEV_WAIT_TIMEOUT = 1, 2
+COLI_INJECT_WITHHOLD_STAGE, COLI_INJECT_BAD_EXPERT_ID = 1, 2
 
 # the in-tree build, the only library this binding loads
 LIB_PATH = _build.LIB
@@ -84,6 +85,8 @@ def lib():
             L.colibri_moe_profile_begin.restype = st
             L.colibri_moe_profile_end.argtypes = [vp, ctypes.POINTER(coli_kernel_time), i32, ctypes.POINTER(i32)]
             L.colibri_moe_profile_end.restype = st
+            L.colibri_moe_debug_inject.argtypes = [vp, i32, ctypes.c_double]
+            L.colibri_moe_debug_inject.restype = st
             L.colibri_moe_last_launch_count.argtypes = [vp]
             L.colibri_moe_last_launch_count.restype = i32
             L.colibri_moe_last_error.argtypes = []
@@ -193,6 +196,12 @@ class Plan:
         return {buf[i].name.decode(): (buf[i].total_ms, buf[i].launches) for i in range(min(n.value, 32))}
 
     profile_end = colibri_moe_profile_end
+
+    def colibri_moe_debug_inject(self, flags: int, wait_limit_ms: float = 0.0):
+        """Failure-path testing: COLI_INJECT_* bits for the next forward calls (0 = off)."""
+        _check(lib().colibri_moe_debug_inject(self.handle, flags, wait_limit_ms))
+
+    debug_inject = colibri_moe_debug_inject
 
     def colibri_moe_last_launch_count(self) -> int:
         return lib().colibri_moe_last_launch_count(self.handle)

@@ -73,6 +73,9 @@ struct coli_moe_plan {
   std::vector<cudaEvent_t> prof_events;  // 2 per kernel launch
   std::vector<int> prof_kernel;          // kernel id per event pair
   int last_launches = 0;
+  // failure-path testing (colibri_moe_debug_inject)
+  int inject = 0;
+  unsigned long long wait_ns = kWaitLimitNs;
 };
 
 static int matrix_row_bytes(int qtype, int K) { return qtype == COLI_Q_INT4_G128 ? K / 2 : K; }
@@ -300,6 +303,8 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   a.hq = reinterpret_cast<uint32_t*>(ws + w.hq);
   a.hqs = reinterpret_cast<int2*>(ws + w.hqs);
   a.y = reinterpret_cast<float*>(ws + w.y);
+  a.wait_ns = plan->wait_ns;
+  a.inject = plan->inject;
 
   const bool prof = plan->prof_calls < plan->prof_max_calls;
   int launches = 0;
@@ -475,6 +480,17 @@ coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out
 }
 
 int colibri_moe_last_launch_count(const coli_moe_plan_t* plan) { return plan ? plan->last_launches : 0; }
+
+coli_status colibri_moe_debug_inject(coli_moe_plan_t* plan, int flags, double wait_limit_ms) {
+  if (!plan) return fail(COLI_EINVAL, "debug_inject: null plan");
+  if (flags & ~(COLI_INJECT_WITHHOLD_STAGE | COLI_INJECT_BAD_EXPERT_ID))
+    return fail(COLI_EINVAL, "debug_inject: unknown flag bits 0x%x", flags);
+  if (!(wait_limit_ms == wait_limit_ms)) return fail(COLI_EINVAL, "debug_inject: wait limit is NaN");
+  plan->inject = flags;
+  plan->wait_ns = wait_limit_ms > 0 ? (unsigned long long)(wait_limit_ms * 1e6) : kWaitLimitNs;
+  if (plan->wait_ns < 1000) plan->wait_ns = 1000;
+  return COLI_OK;
+}
 
 }  // extern "C"
 

@@ -15,14 +15,25 @@ __global__ void combine_kernel(FwdArgs a) {
   if (i4 * 4 >= a.d) return;
   const int P = a.T * a.k;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j = 0; j < a.k; ++j) {
-    const float g = a.topk_w[(size_t)t * a.k + j];
-    const int p = a.pair_of[(size_t)t * a.k + j];
-    const float4 v = *reinterpret_cast<const float4*>(a.y + (size_t)p * a.d + i4 * 4);
-    acc.x = fmaf(g, v.x, acc.x);
-    acc.y = fmaf(g, v.y, acc.y);
-    acc.z = fmaf(g, v.z, acc.z);
-    acc.w = fmaf(g, v.w, acc.w);
+  for (int j0 = 0; j0 < a.k; j0 += 8) {
+    // the slot's row indices and rows are loaded first (independent loads), then summed in slot order
+    int p[8];
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p[i] = j0 + i < a.k ? a.pair_of[(size_t)t * a.k + j0 + i] : -1;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)   // p < 0: pair left out after a rejected expert id (status word set)
+      v[i] = p[i] >= 0 ? *reinterpret_cast<const float4*>(a.y + (size_t)p[i] * a.d + i4 * 4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (p[i] < 0) continue;
+      const float g = a.topk_w[(size_t)t * a.k + j0 + i];
+      acc.x = fmaf(g, v[i].x, acc.x);
+      acc.y = fmaf(g, v[i].y, acc.y);
+      acc.z = fmaf(g, v[i].z, acc.z);
+      acc.w = fmaf(g, v[i].w, acc.w);
+    }
   }
   if (a.has_shared) {
     const float4 v = *reinterpret_cast<const float4*>(a.y + (size_t)(P + t) * a.d + i4 * 4);

@@ -432,7 +432,7 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       if (I4) sr1 = load_scales_int4<DOWN>(ex, u, kb + 2, G);
     }
     const int g = I4 ? (code0 < 0 ? 0 : (code0 >> 7) - kb * kGroupsPerStage) : 0;
-    if (!mbar_wait(bars + stage, phase)) { ok = false; break; }
+    if (!mbar_wait(bars + stage, phase, a.wait_ns)) { ok = false; break; }
     if (code0 >= 0) {
       const uint8_t* sbase = wbuf + stage * kStageBytes + (lane & 15) * 16;
 #pragma unroll
@@ -539,7 +539,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   cursor_load<QT, DOWN>(a, n_routed, n_units, first, prod);
   cons = prod;
   for (int s = 0; s < kDecodeStages && prod.valid; ++s) {
-    if (lane == 0) issue_stage<QT, DOWN>(a, prod, wbuf + s * kStageBytes, bars + s, policy);
+    // failure-path test: warp 0 of CTA 0 withholds its first gate/up stage, so its wait reaches the
+    // (shortened) wait limit and the warp stops with the status set
+    const bool withhold = !DOWN && s == 0 && blockIdx.x == 0 && warp == 0 && (a.inject & COLI_INJECT_WITHHOLD_STAGE);
+    if (lane == 0 && !withhold) issue_stage<QT, DOWN>(a, prod, wbuf + s * kStageBytes, bars + s, policy);
     cursor_next<QT, DOWN>(a, n_routed, n_units, stride, prod);
   }
   int stage = 0;
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
     if (lane == 0) {
       set_status(a.status, COLI_DEV_WAIT_TIMEOUT);
       // drain: wait (bounded) for the stages that may still have a copy in flight
-      for (int s = 0; s < kDecodeStages; ++s) mbar_wait(bars + s, phase ^ (s < stage ? 1u : 0u));
+      for (int s = 0; s < kDecodeStages; ++s) mbar_wait(bars + s, phase ^ (s < stage ? 1u : 0u), a.wait_ns);
     }
     __syncwarp();
   }

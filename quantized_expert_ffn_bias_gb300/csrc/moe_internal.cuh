@@ -117,6 +117,8 @@ struct FwdArgs {
   uint32_t* hq;
   int2* hqs;
   float* y;
+  unsigned long long wait_ns; // limit of every pipeline wait (kWaitLimitNs unless a test shortens it)
+  int inject;                 // COLI_INJECT_* bits of a failure-path test, 0 in normal use
 };
 
 // ---------------------------------------------------------------- launchers (one .cu file each)
@@ -173,7 +175,7 @@ __host__ __device__ constexpr int prefill_raw_row_bytes(int qtype, bool gate_up)
 
 #ifdef __CUDACC__
 
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // give up a pipeline wait after ~1 s
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // default: give up a pipeline wait after ~1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -215,14 +217,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of an mbarrier; false after ~1 s (the caller then
-// records COLI_DEV_WAIT_TIMEOUT and stops using the pipeline).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of an mbarrier; false after limit_ns nanoseconds (the
+// caller then records COLI_DEV_WAIT_TIMEOUT and stops using the pipeline).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((it & 63u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 
@@ -242,12 +244,12 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // Spinning wait for the thread that issues tensor-core instructions: the MMA
 // stream stalls while that thread is busy, and a test_wait on a completed
 // phase returns several times faster than a try_wait.  Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_test_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    if ((it & 255u) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 

@@ -24,8 +24,14 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(FwdArgs a) {
   __syncthreads();
   for (int f = tid; f < P; f += kPermThreads) {
     const int e = a.topk_idx[f];
-    if (e < 0 || e >= E) set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
-    else atomicAdd(&hist[e], 1);
+    if (e < 0 || e >= E) {           // recorded and left out: no row, no output contribution
+      if (blockIdx.x == 0) {
+        set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
+        a.pair_of[f] = -1;
+      }
+    } else {
+      atomicAdd(&hist[e], 1);
+    }
   }
   __syncthreads();
   // exclusive scan over E bins, kPermThreads bins per round

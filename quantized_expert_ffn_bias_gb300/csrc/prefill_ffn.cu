@@ -65,7 +65,10 @@ __global__ void gather_x_f16_kernel(FwdArgs a, __half* xh, int rows) {
     const int r = (int)(i / per_row), c = (int)(i % per_row) * 8;
     const int tok = a.pair_token[r];
     float v[8];
-    if (a.xtype == COLI_X_BF16) {
+    if ((unsigned)tok >= (unsigned)a.T) {   // a row no pair filled (a rejected expert id): zeros
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    } else if (a.xtype == COLI_X_BF16) {
       const uint4 u = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + (size_t)tok * a.d + c);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -389,8 +392,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int kb = 0; kb < nkb; ++kb, ++it) {
           pf_step();
           const int s = it % S;
-          if (it >= S && !mbar_wait(&tma_empty[s], ((it / S) - 1) & 1)) { ok = false; break; }
+          if (it >= S && !mbar_wait(&tma_empty[s], ((it / S) - 1) & 1, a.wait_ns)) { ok = false; break; }
           uint8_t* st = smem + (size_t)s * L::kStageBytes;
+          // failure-path test: CTA 0 withholds its first gate/up stage, so that every role waiting
+          // on it reaches the (shortened) wait limit and the kernel stops with the status set
+          if (GU && it == 0 && blockIdx.x == 0 && (a.inject & COLI_INJECT_WITHHOLD_STAGE)) continue;
           mbar_arrive_expect_tx(&tma_full[s], tx);
           for (int m = 0; m < L::kMats; ++m)
             tma_load_2d_nohint(st + L::kBBytes + m * L::kRawBytes, p.wmaps + (size_t)slot * 3 + (GU ? m : 2),
@@ -404,7 +410,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       // drain: every issued stage must have landed before the CTA can exit
       const int issued = it;
-      for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_full[j % S], (j / S) & 1);
+      for (int j = (issued > S ? issued - S : 0); j < issued; ++j) mbar_wait(&tma_full[j % S], (j / S) & 1, a.wait_ns);
     }
   } else if (warp == 1 || (GU && warp == kPfIssuer2Warp)) {
     // ---------------------------------------------------------------- MMA issuers (gate/up: gate | up)
@@ -420,7 +426,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int acc = GU ? 0 : (tcount & 1);
         const int uses = GU ? tcount : (tcount >> 1);   // earlier tiles that used this accumulator set
         if (uses > 0) {
-          if (!mbar_wait_spin(&acc_empty[acc], (uses - 1) & 1)) { fail_wait(); break; }
+          if (!mbar_wait_spin(&acc_empty[acc], (uses - 1) & 1, a.wait_ns)) { fail_wait(); break; }
           tc_fence_after();
         }
         const uint32_t dacc = tmem + (uint32_t)(acc * kPfN);
@@ -429,7 +435,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           const int as = ia % L::kAStages;
           // a_full also covers the TMA data of the A stage's TMA stages: every dequantising warp
           // waited for their tma_full (raw codes and activations share that barrier) before arriving
-          if (!mbar_wait_spin(&a_full[as], (ia / L::kAStages) & 1)) { ok = false; break; }
+          if (!mbar_wait_spin(&a_full[as], (ia / L::kAStages) & 1, a.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t A = tmem + (uint32_t)(kPfACol + as * L::kAStageCols);
           const int nsub = min(L::kTmaPerA, ntma - j * L::kTmaPerA);
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         umma_commit(&acc_full[acc]);
       }
       // wait for the MMAs in flight before the CTA releases TMEM
-      if (ia > 0) mbar_wait(&a_empty[(ia - 1) % L::kAStages], ((ia - 1) / L::kAStages) & 1);
+      if (ia > 0) mbar_wait(&a_empty[(ia - 1) % L::kAStages], ((ia - 1) / L::kAStages) & 1, a.wait_ns);
     }
   } else if (warp < 2 + kPfEpWarps) {
     // ---------------------------------------------------------------- epilogue (warps 2..5)
@@ -462,7 +468,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       tile_info(t, slot, row0, ntok, mb, K);
       const int acc = GU ? 0 : (tcount & 1);
       const int uses = GU ? tcount : (tcount >> 1);
-      if (!mbar_wait(&acc_full[acc], uses & 1)) { fail_wait(); break; }
+      if (!mbar_wait(&acc_full[acc], uses & 1, a.wait_ns)) { fail_wait(); break; }
       tc_fence_after();
       const DevExpert& ex = a.experts[slot];
       const int orow = mb * kPfM + sp * 32 + lane;  // weight row of this thread (TMEM lane)
@@ -559,7 +565,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int j = 0; j < nA && ok; ++j, ++ia) {
         const int as = ia % L::kAStages;
         if (ia >= L::kAStages) {
-          if (!mbar_wait(&a_empty[as], ((ia / L::kAStages) - 1) & 1)) { ok = false; break; }
+          if (!mbar_wait(&a_empty[as], ((ia / L::kAStages) - 1) & 1, a.wait_ns)) { ok = false; break; }
           tc_fence_after();
         }
         const int nsub = min(L::kTmaPerA, nkb - j * L::kTmaPerA);
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           zz = (0x6400u | zraw) * 0x10001u;          // half2(1024 + z)
           zzh = (0x5400u | (zraw << 4)) * 0x10001u;  // half2(64 + z)
         }
-        if (!mbar_wait(&tma_full[s], (it / S) & 1)) { ok = false; break; }
+        if (!mbar_wait(&tma_full[s], (it / S) & 1, a.wait_ns)) { ok = false; break; }
         const uint8_t* raw = smem + (size_t)s * L::kStageBytes + L::kBBytes + (GU ? mat_i * L::kRawBytes : 0) +
                              r * L::kRawRow;
 #pragma unroll

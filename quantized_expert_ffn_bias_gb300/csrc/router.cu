@@ -308,6 +308,8 @@ __device__ void topk_token(const FwdArgs& a, int t, float* u, float* s) {
   for (int e = lane; e < a.E; e += 32) router_scores(a, t, e, s[e], u[e]);
   __syncwarp();
   topk_select(a, t, u, s, nullptr);
+  // failure-path test: an out-of-range id for the grouping step to reject
+  if ((a.inject & COLI_INJECT_BAD_EXPERT_ID) && t == 0 && lane == 0) a.topk_idx[0] = -1;
 }
 
 __global__ void __launch_bounds__(kTopkWarps * 32) router_topk_kernel(FwdArgs a) {
@@ -463,13 +465,28 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
     }
   }
   __syncthreads();
+  const int E = a.E, P = a.T * a.k;
+  // a failure-path test plants an out-of-range id here; any id outside [0, E) is recorded in the
+  // status word and mapped to E, which sorts after every expert and is left out of the grouping
+  if ((a.inject & COLI_INJECT_BAD_EXPERT_ID) && tid == 0) sidx[0] = -1;
+  __syncthreads();
+  for (int f = tid; f < P; f += kRouteThreads) {
+    if (sidx[f] < 0 || sidx[f] >= E) {
+      set_status(a.status, COLI_DEV_BAD_EXPERT_ID);
+      sidx[f] = E;
+    }
+  }
+  __syncthreads();
   // (5) grouping of the P = T*k <= 256 pairs (stable counting sort by expert id),
   //     by direct counting over the pairs: position of pair f = pairs with a lower
   //     expert id, plus earlier pairs of the same expert
-  const int E = a.E, P = a.T * a.k;
   for (int f = tid; f < P; f += kRouteThreads) {
     const int e = sidx[f];
-    if (e < 0 || e >= E) { set_status(a.status, COLI_DEV_BAD_EXPERT_ID); continue; }
+    if (e == E) {                    // left out: no row, no output contribution
+      a.pair_of[f] = -1;
+      hist[f] = 0;
+      continue;
+    }
     int pos = 0, first = 1;
     for (int g = 0; g < P; ++g) {
       const int eg = sidx[g];

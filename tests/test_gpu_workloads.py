@@ -35,6 +35,31 @@ def _sample(T, n, seed):
     return np.sort(np.random.default_rng(seed).choice(T, size=n, replace=False)).astype(np.int32)
 
 
+CHUNK = 128   # tokens per tensor-core chunk of one expert
+
+
+def _chunk_cover(dl, T: int, has_shared: bool, seed: int, n_heavy: int = 2):
+    """Tokens whose outputs reach every 128-token chunk of the n_heavy most loaded experts (one token of
+    each chunk, from the GPU's own grouping of this input) and the shared expert's last chunk.  Returns
+    (tokens, description of the chosen chunks)."""
+    _, _, _, off, pt, _ = dl.routing(T)
+    loads = np.diff(off)
+    heavy = np.argsort(-loads, kind="stable")[:n_heavy]
+    rng = np.random.default_rng(seed)
+    toks, desc = set(), []
+    for e in heavy:
+        n_ch = (int(loads[e]) + CHUNK - 1) // CHUNK
+        for c in range(n_ch):
+            lo, hi = int(off[e]) + c * CHUNK, min(int(off[e + 1]), int(off[e]) + (c + 1) * CHUNK)
+            toks.add(int(pt[rng.integers(lo, hi)]))
+        desc.append(f"expert {int(e)}: {int(loads[e])} tokens, {n_ch} chunks")
+    if has_shared:                 # the shared expert's rows are the tokens in order
+        last = (T - 1) // CHUNK
+        toks.add(int(rng.integers(last * CHUNK, T)))
+        desc.append(f"shared expert: chunk {last} (tokens {last * CHUNK}..{T - 1})")
+    return np.array(sorted(toks), np.int32), "; ".join(desc)
+
+
 def _release(dl):
     import torch
     dl.close()
@@ -74,16 +99,19 @@ def test_mtp_verify_T3_shared_and_overlap():
 
 
 def test_prefill_T2048_skewed():
-    from harness.device import DeviceLayer
+    from harness.device import DeviceLayer, to_dev
     w = H.WORKLOADS["prefill"]
     layer = w.layer(0)
     dl = DeviceLayer(layer, 2048)
     x = w.x(2048, 0)
-    rep = run_layer_parity(dl, layer, x, tokens=_sample(2048, 48, 3))
+    dl.forward(to_dev(x, dl.device))
+    cover, desc = _chunk_cover(dl, 2048, True, 5)
+    toks = np.union1d(_sample(2048, 48, 3), cover).astype(np.int32)
+    rep = run_layer_parity(dl, layer, x, tokens=toks)
     off = dl.routing(2048)[3]
     loads = np.diff(off)
     print(f"prefill: loads min={loads.min()} max={loads.max()} idle={int((loads == 0).sum())} "
-          f"rel_l2={rep.rel_l2:.2e} near_ties={rep.near_ties}")
+          f"rel_l2={rep.rel_l2:.2e} near_ties={rep.near_ties}; {len(toks)} outputs checked, covering {desc}")
     assert loads.max() > 400
     _release(dl)
 
@@ -112,9 +140,12 @@ def test_stacked_six_layers_T256():
         assert diff.mean() < 1e-3, f"layer {l}: rmsnorm differs on {diff.sum()} elements"
         if diff.any():
             assert np.all(np.abs(n_np[diff].astype(np.int32) - n_ref[diff].astype(np.int32)) == 1)
-        rep = run_layer_parity(dl, layer, n_np, tokens=toks, residual=h_np.astype(np.float32))
+        dl.forward(n, residual=h)
+        cover, desc = _chunk_cover(dl, T, False, 10 + l)
+        lt = np.union1d(toks, cover).astype(np.int32)
+        rep = run_layer_parity(dl, layer, n_np, tokens=lt, residual=h_np.astype(np.float32))
         print(f"stacked layer {l} ({'int4' if layer.qtype == 0 else 'int8'}): rel_l2={rep.rel_l2:.2e} "
-              f"near_ties={rep.near_ties}")
+              f"near_ties={rep.near_ties}; {len(lt)} outputs checked, covering {desc}")
         h_next = torch.empty_like(h)
         dl.forward(n, out=h_next, residual=h)
         torch.cuda.synchronize()

@@ -2,16 +2,19 @@
 
 It exists for callers that cannot allocate device memory (a host framework that
 owns every allocation, or code regions where allocating is not allowed).  The
-test checks it against the ordinary forward (same kernels, caller workspace) on
-two calls in a row, with the output tolerances of the parity tests, and that a
-plan too large for the static scratch is refused.  This file is collected last
+tests check it against the ordinary forward (same kernels, caller workspace) on
+two calls in a row and against the oracle, with the output tolerances of the
+parity tests; run a plan whose workspace is just under the 8 MiB limit (the
+tensor-core path); and check that a plan too large for the static scratch is
+refused.  This file is collected last
 so that a failure here never hides the other tests.
 """
 import numpy as np
 import pytest
 
 import harness as H
-from tests.gpu_parity import MAX_ABS_TOL, REL_L2_TOL, rel_l2
+import oracle as O
+from tests.gpu_parity import MAX_ABS_TOL, REL_L2_TOL, check_output, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -46,6 +49,56 @@ def test_noalloc_forward_matches_workspace_forward(torch_cuda):
         assert np.isfinite(a).all()
         assert rel_l2(a, b) <= REL_L2_TOL
         assert np.abs(a - b).max() <= MAX_ABS_TOL * np.sqrt(np.mean(b ** 2))
+        # and against the oracle (tokens whose expert choice is not a near-tie)
+        xn = H.gen_x(31, call, T, 1024, H.X_BF16)
+        orc = O.Oracle(layer)
+        gap = orc.route(xn)[2]
+        toks = np.flatnonzero(gap >= O.NEAR_TIE).astype(np.int32)
+        ref_o = orc.forward(xn, tokens=toks)
+        if res is not None:
+            ref_o = ref_o + res.cpu().numpy().astype(np.float64)[toks]
+        check_output(a[toks], ref_o)
+    dl.close()
+
+
+def _largest_T_max_within(limit: int, **desc) -> int:
+    import quantized_expert_ffn_bias_gb300 as coli
+    lo, hi = 1, 1 << 14                 # plans are host-only: search the largest T_max that fits
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        p = coli.Plan(T_max=mid, **desc)
+        fits = p.workspace_bytes <= limit
+        p.close()
+        lo, hi = (mid, hi) if fits else (lo, mid - 1)
+    return lo
+
+
+def test_noalloc_plan_at_the_scratch_limit(torch_cuda):
+    """A plan whose workspace is just under 8 MiB (here a tensor-core sized token count), called after a
+    workspace forward of another plan, matches the oracle on every token."""
+    torch = torch_cuda
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+    layer = H.gen_layer(32, 0, d=1024, F=512, E=16, k=4, rho=2.5, qtype=H.Q_INT4_G128, bias="uniform:0.1",
+                        F_shared=256)
+    desc = dict(d=1024, d_ff=512, E=16, k=4, routed_scale=2.5, qtype=coli.COLI_Q_INT4_G128,
+                xtype=coli.COLI_X_BF16, has_shared=True, shared_d_ff=256)
+    T_max = _largest_T_max_within(8 << 20, **desc)
+    assert T_max > 8                    # the limit is reached on the tensor-core path
+    dl = DeviceLayer(layer, T_max)
+    assert (8 << 20) - (1 << 16) < dl.plan.workspace_bytes <= (8 << 20)
+    x = H.gen_x(32, 0, T_max, 1024, H.X_BF16)
+    xd = to_dev(x, dl.device)
+    dl.forward(xd)                      # leaves routing state of its own in the caller workspace
+    out = torch.full((T_max, 1024), float("nan"), device=dl.device)
+    dl.plan.forward_noalloc(T_max, xd, dl.router_w, dl.bias, out, stream=torch.cuda.current_stream(dl.device))
+    torch.cuda.synchronize()
+    a = out.cpu().numpy().astype(np.float64)
+    orc = O.Oracle(layer)
+    gap = orc.route(x)[2]
+    toks = np.flatnonzero(gap >= O.NEAR_TIE).astype(np.int32)
+    check_output(a[toks], orc.forward(x, tokens=toks))
+    print(f"noalloc at T_max={T_max}: workspace {dl.plan.workspace_bytes} of {8 << 20} bytes")
     dl.close()
 
 
