@@ -121,6 +121,12 @@ typedef struct coli_moe_plan coli_moe_plan_t;
 
 /*
  * Validate `desc` and create a plan (host memory only; no CUDA call).
+ * The description fixes the layer of the "25GB RAM runs 744B GLM-5.2" page:
+ * E routed experts of which k are chosen per token (section 3.1), int4 or
+ * int8 weights with per-channel scale and zero point ("Colibri walkthrough"
+ * page, section 3.4), an optional resident shared expert (section 2).  The
+ * workspace holds the batch-union grouping of section 3.4: per-expert pair
+ * lists, so that each chosen expert is streamed once for all its tokens.
  * *workspace_bytes receives the size of the device workspace a forward call
  * needs for up to T_max tokens (256-byte aligned base required).
  * Errors: COLI_EINVAL (null argument, bad sizes), COLI_EUNSUPPORTED.
@@ -128,7 +134,10 @@ typedef struct coli_moe_plan coli_moe_plan_t;
 COLI_API coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, size_t* workspace_bytes);
 
 /*
- * Bind the expert weights (the resident "expert slots") to a plan on the
+ * Bind the expert weights (the resident "expert slots" of the "Colibri
+ * walkthrough" page, section 3.1; here every expert of the layer is resident
+ * in device memory, one contiguous block per expert matrix as in its
+ * section 4.2 layout) to a plan on the
  * current device.  experts: HOST array [E] of descriptors holding device
  * pointers; shared: HOST pointer to one descriptor, or NULL when the plan has
  * no shared expert.  The weights themselves are not copied: they must stay
@@ -141,7 +150,9 @@ COLI_API coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t
 COLI_API coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* experts, const coli_expert* shared);
 
 /*
- * One layer forward for T tokens (1 <= T <= T_max), asynchronous on stream.
+ * One layer forward for T tokens (1 <= T <= T_max), asynchronous on stream:
+ * steps 1-6 at the top of this header ("25GB RAM runs 744B GLM-5.2" page,
+ * sections 3.1, 3.4 and 4.3; "Colibri walkthrough" page, section 3.4).
  *   x         device [T][d], bf16 or fp32 per desc.xtype (16-byte aligned).
  *   router_w  device float [E][d] (16-byte aligned).
  *   bias      device float [E]: selection-only router bias.
@@ -188,7 +199,9 @@ COLI_API coli_status colibri_moe_forward_noalloc(const coli_moe_plan_t* plan, in
 COLI_API coli_status colibri_moe_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, void* stream);
 
 /*
- * Copy the routing state of the last forward that used `workspace` into
+ * Routing check (the pages ask for exact routing: "25GB RAM runs 744B
+ * GLM-5.2" page, section 4.3, DeepSeek-V3 sigmoid router, selection and
+ * scaling).  Copy the routing state of the last forward that used `workspace` into
  * caller buffers (device pointers, any may be NULL), asynchronously on stream:
  *   topk_idx int32 [T][k]  chosen experts, ascending ids per token
  *   topk_w   float [T][k]  gate weights in the same order
