@@ -32,6 +32,7 @@ X_F32 = 1
 
 # stream tags
 _TAG_X, _TAG_ROUTER, _TAG_BIAS, _TAG_GATE, _TAG_UP, _TAG_DOWN, _TAG_PERM = 1, 2, 3, 4, 5, 6, 7
+_TAG_IDX_Q, _TAG_IDX_W, _TAG_IDX_K = 8, 9, 10
 SHARED_ID = 1 << 20  # expert index used for the shared expert's streams
 
 
@@ -292,3 +293,34 @@ WORKLOADS = {
     "stacked": Workload("stacked", 4, (256,), 7168, 2048, 256, 8, 2.5,
                         (Q_INT4_G128, Q_INT8_PC) * 3, X_BF16, "zero", rmsnorm_eps=1e-6),
 }
+
+
+# --------------------------------------------------------------------------- sparse-attention key selection
+
+@dataclasses.dataclass(frozen=True)
+class IndexerWorkload:
+    """Inputs of the key-selection step of sparse attention: T query tokens at the end of a context of L
+    cached keys; H indexer heads of dimension d; the topk highest-scoring causal keys are kept
+    ("25GB RAM runs 744B GLM-5.2" page, section 3.3: top-2048 causal keys per layer).  The shapes H = 64,
+    d = 128 follow the DeepSeek-V3.2 indexer that the page cites; q and k are bf16 N(0, 1), the per-head
+    weights w fp32 N(0, 1/H)."""
+    name: str
+    seed: int
+    T: tuple
+    L: int
+    H: int
+    d: int
+    topk: int
+
+    def q(self, T: int, stream: int = 0) -> np.ndarray:
+        return to_bf16_bits(normal(key(self.seed, _TAG_IDX_Q, stream), T * self.H * self.d).reshape(T, self.H, self.d))
+
+    def w(self, T: int, stream: int = 0) -> np.ndarray:
+        return normal(key(self.seed, _TAG_IDX_W, stream), T * self.H, 0.0, self.H ** -0.5).reshape(T, self.H)
+
+    def keys(self, L: int | None = None, stream: int = 0) -> np.ndarray:
+        L = self.L if L is None else L
+        return to_bf16_bits(normal(key(self.seed, _TAG_IDX_K, stream), L * self.d).reshape(L, self.d))
+
+
+INDEXER = IndexerWorkload("indexer", 5, (1, 4), 65536, 64, 128, 2048)

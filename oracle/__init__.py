@@ -22,6 +22,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle_moe.c")
+_SRC_INDEXER = os.path.join(_HERE, "oracle_indexer.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle_moe.so")
 _lock = threading.Lock()
@@ -49,10 +50,11 @@ class _Desc(ctypes.Structure):
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP over tokens, no FMA contraction)."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB_PATH) or \
+            os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(_SRC), os.path.getmtime(_SRC_INDEXER)):
         tmp = _LIB_PATH + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp, _SRC, _SRC_INDEXER, "-lm"])
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -75,6 +77,11 @@ def _bind(L):
                                   ctypes.POINTER(_Expert), vp, i32, vp, vp, i32]
     L.orc_moe_forward.restype = i32
     L.orc_rmsnorm_bf16.argtypes = [i32, vp, f64, vp]
+    if hasattr(L, "orc_indexer_scores"):
+        L.orc_indexer_scores.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, i32]
+        L.orc_indexer_scores.restype = i32
+        L.orc_indexer_topk.argtypes = [i32, i32, i32, vp, vp, vp]
+        L.orc_indexer_topk.restype = i32
     return L
 
 
@@ -262,3 +269,33 @@ def stacked_forward(layers, x: np.ndarray, eps: float, tokens=None, nthreads: in
         inputs.append(nb)
         h = h + Oracle(layer, L=L).forward(nb, nthreads=nthreads)
     return (h, inputs) if return_layer_inputs else h
+
+
+# --------------------------------------------------------------------------- sparse-attention key selection
+
+def indexer_scores(q: np.ndarray, w: np.ndarray, keys: np.ndarray, pos0: int, nthreads: int | None = None,
+                   L=None) -> np.ndarray:
+    """I[t][s] = sum_j w[t][j] * relu(q[t][j] . k[s]) (float64 [T, L]); -inf where s > pos0 + t.
+    q: bf16 bits [T, H, d]; w: float32 [T, H]; keys: bf16 bits [L, d]."""
+    q = np.ascontiguousarray(q, np.uint16)
+    w = np.ascontiguousarray(w, np.float32)
+    keys = np.ascontiguousarray(keys, np.uint16)
+    T, H, d = q.shape
+    Lk = keys.shape[0]
+    assert keys.shape[1] == d and w.shape == (T, H)
+    out = np.zeros((T, Lk), np.float64)
+    if lib(L).orc_indexer_scores(T, Lk, H, d, pos0, _p(q), _p(w), _p(keys), _p(out), nthreads or default_threads()):
+        raise ValueError("orc_indexer_scores: bad sizes")
+    return out
+
+
+def indexer_topk(scores: np.ndarray, topk: int, L=None):
+    """(selected keys int32 [T, topk] ascending, -1 padded; gap float64 [T] between the topk-th and the
+    (topk+1)-th largest visible score) of float64 scores [T, L]."""
+    scores = np.ascontiguousarray(scores, np.float64)
+    T, Lk = scores.shape
+    idx = np.zeros((T, topk), np.int32)
+    gap = np.zeros(T, np.float64)
+    if lib(L).orc_indexer_topk(T, Lk, topk, _p(scores), _p(idx), _p(gap)):
+        raise ValueError("orc_indexer_topk failed")
+    return idx, gap
