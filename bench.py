@@ -8,11 +8,13 @@ line and the others under ``variants``:
   prefill T=2048    the same plus a shared expert, Zipf-skewed router bias
   stacked T=256     six layers (int4 / int8 alternating) with RMSNorm and residual, 51.4 GB resident
 A step is one full forward (router, grouping, gate/up + SwiGLU, down, combine; for the stacked workload
-the whole stack) on a fresh x, so routing differs every step; every expert set is far larger than L2.
+the whole stack; for the indexer one scoring + selection of every query token) on a fresh x, so routing differs every step; every expert set is far larger than L2.
 Each entry carries its own roofline, end-to-end figure, CPU baseline (the oracle), clock record and
 routing statistics (near-tie tokens, unique experts per step).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked]
+  indexer T=1 / T=4 sparse-attention key selection: 64 heads of 128, 65,536 cached keys, top-2048
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked|indexer]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores (CPU baseline arm)
 
 Prints one JSON line (rank 0).
@@ -457,6 +459,117 @@ def bench_stacked(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
     return line, gen_s
 
 
+def bench_indexer(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
+    """Sparse-attention key selection (lightning indexer scores + top-2048) for T query tokens at the end of
+    a context of 65,536 cached keys.  Each step uses the key cache of the next of 16 layers (16 x 16.8 MB,
+    larger than L2), as a decode step visits every layer's cache once."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import to_dev
+
+    w = H.INDEXER
+    Ts = (args.tokens,) if args.tokens else w.T
+    L = w.L
+    n_sets = 16
+    t0 = time.time()
+    keys = [to_dev(w.keys(L, 100 + i), dev) for i in range(n_sets)]
+    gen_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+    K, W = args.steps, args.warmup
+    pk = peaks()
+    frags = {}
+    for T in Ts:
+        qs = [to_dev(w.q(T, 1000 + i), dev) for i in range(K + W)]
+        ws_ = [to_dev(w.w(T, 1000 + i), dev) for i in range(K + W)]
+        nbytes = coli.colibri_indexer_workspace_size(T, L)
+        wsp = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        out = torch.empty((T, w.topk), dtype=torch.int32, device=dev)
+        state = {"i": 0}
+
+        def step(i):
+            coli.colibri_indexer_topk(T, L, L - T, w.H, w.d, w.topk, qs[i], ws_[i], keys[i % n_sets], out, wsp,
+                                      nbytes, stream)
+            return out
+
+        def timed(fn):
+            for i in range(W):
+                fn(i)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                torch.distributed.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(K):
+                fn(W + i)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if world > 1:
+                torch.distributed.barrier()
+            return e0.elapsed_time(e1)
+
+        with ClockSampler(dev.index) as clk:
+            ms = timed(step)
+        ms_sc = timed(lambda i: coli.colibri_indexer_scores(T, L, L - T, w.H, w.d, qs[i], ws_[i], keys[i % n_sets],
+                                                            wsp, nbytes, stream))
+        ms_sel = timed(lambda i: coli.colibri_indexer_select(T, L, L - T, w.topk, out, wsp, nbytes, stream))
+        assert coli.colibri_indexer_check_status(wsp, stream) == 0
+        # end to end: the query heads and weights from pinned host memory, the selection back
+        qh = [qs[W + i].cpu().pin_memory() for i in range(K)]
+        wh = [ws_[W + i].cpu().pin_memory() for i in range(K)]
+        oh = torch.empty((K, T, w.topk), dtype=torch.int32).pin_memory()
+        qd, wd = torch.empty_like(qs[0]), torch.empty_like(ws_[0])
+        torch.cuda.synchronize(dev)
+        te = time.perf_counter()
+        for i in range(K):
+            qd.copy_(qh[i], non_blocking=True)
+            wd.copy_(wh[i], non_blocking=True)
+            coli.colibri_indexer_topk(T, L, L - T, w.H, w.d, w.topk, qd, wd, keys[(W + i) % n_sets], out, wsp,
+                                      nbytes, stream)
+            oh[i].copy_(out, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(time.perf_counter() - te, dev)
+        ms, ms_sc, ms_sel = max_over_ranks(ms, dev), max_over_ranks(ms_sc, dev), max_over_ranks(ms_sel, dev)
+        n_groups = (T + 3) // 4
+        # algorithmic bytes of the score kernel(s): the keys once per launch group, the query heads and
+        # weights, the scores written
+        alg = n_groups * L * w.d * 2 + T * (w.H * w.d * 2 + w.H * 4) + T * L * 4
+        ach = alg / (ms_sc / K * 1e-3) / 1e9
+        cpu = None
+        if want_cpu and T == Ts[0]:
+            import oracle as O
+            cores = O.default_threads()
+            qc, wc, kc = w.q(1, 77), w.w(1, 77), w.keys(L, 77)
+            tc0 = time.perf_counter()
+            n = 0
+            while time.perf_counter() - tc0 < cpu_budget_s:
+                O.indexer_topk(O.indexer_scores(qc, wc, kc, L - 1, nthreads=cores), w.topk)
+                n += 1
+            dt = time.perf_counter() - tc0
+            cpu = {"value": n / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                   "sample": f"{n} query tokens over {L} keys (64 heads of 128, top-{w.topk}), fp64 scores over "
+                             f"{cores} threads, {dt:.1f} s"}
+        frags[T] = {
+            "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s", "ms_per_step": ms / K,
+            "roofline": {"bound": "hbm", "kernel": "indexer_scores", "achieved": ach, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                         "algorithmic_bytes_per_launch": alg},
+            "kernel_ms_per_step": {"indexer_scores": ms_sc / K, "indexer_select": ms_sel / K},
+            "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s",
+                    "h2d_bytes_per_step": qh[0].numel() * qh[0].element_size() + wh[0].numel() * 4,
+                    "d2h_bytes_per_step": T * w.topk * 4},
+            "gpu_launches": K * (n_groups + 1),
+            "clocks": clk.summary(),
+            "config": {"workload": f"indexer: sparse-attention key selection (scores + top-{w.topk}) for T={T} "
+                                   f"query tokens over {L} cached keys", "heads": w.H, "head_dim": w.d,
+                       "topk": w.topk, "keys": L, "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": f"inputs larger than L2: {n_sets} key caches of {L * w.d * 2 / 1e6:.1f} MB cycled"},
+            "cpu_baseline": cpu,
+        }
+    del keys
+    torch.cuda.empty_cache()
+    return frags, gen_s
+
+
 def cpu_baseline(w, layer, T: int, budget_s: float):
     """The oracle as it stands on this host's cores (OpenMP over tokens), on a bounded sample of the
     workload's tokens: calls of `cores` tokens each until `budget_s` seconds have passed."""
@@ -522,7 +635,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="all", choices=["all", "decode", "mtp_verify", "prefill", "stacked"],
+    ap.add_argument("--workload", default="all",
+                    choices=["all", "decode", "mtp_verify", "prefill", "stacked", "indexer"],
                     help="all (default): decode T=1 as the headline with decode T=4, MTP verify, prefill and the "
                          "stacked layers as variants; otherwise that workload alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -544,11 +658,15 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl")
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    names = ["decode", "mtp_verify", "prefill", "stacked"] if args.workload == "all" else [args.workload]
+    names = ["decode", "mtp_verify", "prefill", "stacked", "indexer"] if args.workload == "all" else [args.workload]
     results, gen_total = [], 0.0
     for name in names:
         budget = 10.0 if name == names[0] else 6.0
-        if name == "stacked":
+        if name == "indexer":
+            frags, gen_s = bench_indexer(args, dev, world, want_cpu, budget)
+            for T, fr in frags.items():
+                results.append((f"indexer T={T}", "indexer", T, fr))
+        elif name == "stacked":
             line, gen_s = bench_stacked(args, dev, world, want_cpu, budget)
             ws, T_s, _ = workload_setup("stacked", args.experts, args.tokens)
             results.append((f"stacked {ws.n_layers} layers T={T_s}", "stacked", None, line))
@@ -561,10 +679,11 @@ def main():
     if rank != 0:
         return
     head_label, head_name, head_T, head = results[0]
-    w = H.WORKLOADS[head_name]
     line = {"metric": METRIC}
     line.update({k: head[k] for k in VARIANT_KEYS if k in head})
-    if head_name == "stacked":
+    if head_name == "indexer":
+        dtype = "bf16 tensor-core operands, f32 accumulate"
+    elif head_name == "stacked":
         dtype = "int4/int8-weights, fp16 tensor-core operands, f32 accumulate"
     elif head_T is not None and head_T > 8:
         dtype = "int4-weights, fp16 tensor-core operands, f32 accumulate"

@@ -267,6 +267,42 @@ typedef struct {
 COLI_API coli_status colibri_moe_profile_begin(coli_moe_plan_t* plan, int max_calls);
 COLI_API coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out, int max_kernels, int* n_kernels);
 
+/*
+ * Key selection of sparse attention (DSA "lightning indexer" and top-k):
+ * "25GB RAM runs 744B GLM-5.2" page, section 3.3: each layer keeps only the
+ * top-2048 causal keys for attention; section 4.4: a light indexer scores the
+ * earlier keys, then the top-k entries are selected.  The pages give no
+ * scoring formula; this library computes that of the DeepSeek-V3.2 indexer
+ * the page cites:
+ *   I[t][s] = sum_{j < H} w[t][j] * relu(q[t][j] . k[s]),
+ * for the keys s <= pos0 + t (and s < L) that query t, at position pos0 + t,
+ * sees; the topk largest are kept, a tie going to the lower key index.
+ *   q        device bf16 [T][H][d] (16-byte aligned); w device float [T][H];
+ *   keys     device bf16 [L][d] (16-byte aligned);
+ *   topk_idx device int32 [T][topk]: the selected keys in ascending order,
+ *            -1 padded when a query sees fewer than topk keys.
+ *   workspace device, >= colibri_indexer_workspace_size(T, L) bytes, 256-byte
+ *            aligned.  Layout: int32 status word at offset 0; the fp32 scores
+ *            [T][L] at offset 256 (-infinity where a key is not visible);
+ *            then a 65536-bin histogram of each query's scores (selection).
+ * This build serves H = 64 heads of d = 128 and L <= 131072 keys
+ * (COLI_EUNSUPPORTED otherwise).
+ * Asynchronous on stream; errors: COLI_EINVAL, COLI_EALIGN, COLI_EWORKSPACE,
+ * COLI_EUNSUPPORTED, COLI_ECUDA.  colibri_indexer_check_status reads the
+ * status word (COLI_DEV_WAIT_TIMEOUT if a pipeline wait gave up).
+ */
+COLI_API coli_status colibri_indexer_workspace_size(int T_max, int L_max, size_t* bytes);
+COLI_API coli_status colibri_indexer_topk(int T, int L, int pos0, int H, int d, int topk, const void* q, const float* w,
+                                          const void* keys, int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                                          void* stream);
+COLI_API coli_status colibri_indexer_check_status(const void* workspace, int32_t* device_status, void* stream);
+/* The two steps of colibri_indexer_topk on their own (same arguments and
+ * workspace): the scores into the workspace, then the selection from them. */
+COLI_API coli_status colibri_indexer_scores(int T, int L, int pos0, int H, int d, const void* q, const float* w,
+                                            const void* keys, void* workspace, size_t workspace_bytes, void* stream);
+COLI_API coli_status colibri_indexer_select(int T, int L, int pos0, int topk, int32_t* topk_idx, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* Number of kernel launches the last forward call of this plan issued. */
 COLI_API int colibri_moe_last_launch_count(const coli_moe_plan_t* plan);
 

@@ -87,6 +87,16 @@ def lib():
             L.colibri_moe_profile_end.restype = st
             L.colibri_moe_debug_inject.argtypes = [vp, i32, ctypes.c_double]
             L.colibri_moe_debug_inject.restype = st
+            L.colibri_indexer_workspace_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
+            L.colibri_indexer_workspace_size.restype = st
+            L.colibri_indexer_topk.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
+            L.colibri_indexer_topk.restype = st
+            L.colibri_indexer_scores.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+            L.colibri_indexer_scores.restype = st
+            L.colibri_indexer_select.argtypes = [i32, i32, i32, i32, vp, vp, sz, vp]
+            L.colibri_indexer_select.restype = st
+            L.colibri_indexer_check_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
+            L.colibri_indexer_check_status.restype = st
             L.colibri_moe_last_launch_count.argtypes = [vp]
             L.colibri_moe_last_launch_count.restype = i32
             L.colibri_moe_last_error.argtypes = []
@@ -124,6 +134,39 @@ def colibri_moe_last_error() -> str:
 
 def colibri_moe_rmsnorm_bf16(h, T: int, d: int, eps: float, out, stream=None):
     _check(lib().colibri_moe_rmsnorm_bf16(_ptr(h), T, d, eps, _ptr(out), _stream(stream)))
+
+
+def colibri_indexer_workspace_size(T_max: int, L_max: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().colibri_indexer_workspace_size(T_max, L_max, ctypes.byref(n)))
+    return n.value
+
+
+def colibri_indexer_topk(T: int, L: int, pos0: int, H: int, d: int, topk: int, q, w, keys, topk_idx, workspace,
+                         workspace_bytes: int, stream=None):
+    """Sparse-attention key selection (see the header): scores in the workspace, selection in topk_idx."""
+    _check(lib().colibri_indexer_topk(T, L, pos0, H, d, topk, _ptr(q), _ptr(w), _ptr(keys), _ptr(topk_idx),
+                                      _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def colibri_indexer_scores(T: int, L: int, pos0: int, H: int, d: int, q, w, keys, workspace, workspace_bytes: int,
+                           stream=None):
+    _check(lib().colibri_indexer_scores(T, L, pos0, H, d, _ptr(q), _ptr(w), _ptr(keys), _ptr(workspace),
+                                        workspace_bytes, _stream(stream)))
+
+
+def colibri_indexer_select(T: int, L: int, pos0: int, topk: int, topk_idx, workspace, workspace_bytes: int,
+                           stream=None):
+    _check(lib().colibri_indexer_select(T, L, pos0, topk, _ptr(topk_idx), _ptr(workspace), workspace_bytes,
+                                        _stream(stream)))
+
+
+def colibri_indexer_check_status(workspace, stream=None) -> int:
+    v = ctypes.c_int32()
+    rc = lib().colibri_indexer_check_status(_ptr(workspace), ctypes.byref(v), _stream(stream))
+    if rc not in (COLI_OK, COLI_EDEVICE):
+        _check(rc)
+    return v.value
 
 
 def qmat(q, scale, zp) -> coli_qmat:

@@ -481,6 +481,118 @@ coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out
 
 int colibri_moe_last_launch_count(const coli_moe_plan_t* plan) { return plan ? plan->last_launches : 0; }
 
+// ------------------------------------------------------------------ sparse-attention key selection
+
+// status | scores [T][L] | counts [T] | histogram [T][65536] | coarse histogram [T][2048] |
+// bitmask [T][ceil(L/32)] | candidates [T][2048] x 2   (counts and histograms adjoin: one clear covers them)
+static size_t indexer_ws_bytes(int T, int L) {
+  return 256 + align_up((size_t)T * (size_t)L * 4, 256) + align_up((size_t)T * 4, 256) + (size_t)T * 65536 * 4 +
+         (size_t)T * 2048 * 4 + align_up((size_t)T * ((L + 31) / 32) * 4, 256) + (size_t)T * 2048 * 8;
+}
+
+coli_status colibri_indexer_workspace_size(int T_max, int L_max, size_t* bytes) {
+  if (!bytes || T_max < 1 || L_max < 1) return fail(COLI_EINVAL, "indexer_workspace_size: bad argument");
+  *bytes = indexer_ws_bytes(T_max, L_max);
+  return COLI_OK;
+}
+
+static coli_status indexer_call(int steps, int T, int L, int pos0, int H, int d, int topk, const void* q,
+                                const float* w, const void* keys, int32_t* topk_idx, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (((steps & 1) && (!q || !w || !keys)) || ((steps & 2) && !topk_idx) || !workspace)
+    return fail(COLI_EINVAL, "indexer_topk: null pointer");
+  if (T < 1 || L < 1 || topk < 1 || pos0 < 0) return fail(COLI_EINVAL, "indexer_topk: need T, L, topk >= 1, pos0 >= 0");
+  if (H != 64 || d != 128)
+    return fail(COLI_EUNSUPPORTED, "indexer_topk: this build serves 64 heads of 128 (got %d x %d)", H, d);
+  if ((long long)T * L > (1LL << 31)) return fail(COLI_EUNSUPPORTED, "indexer_topk: T*L too large");
+  if (L > (1 << 17)) return fail(COLI_EUNSUPPORTED, "indexer_topk: this build selects among at most 131072 keys");
+  if (workspace_bytes < indexer_ws_bytes(T, L))
+    return fail(COLI_EWORKSPACE, "indexer_topk: workspace %zu bytes < required %zu", workspace_bytes,
+                indexer_ws_bytes(T, L));
+  if (!aligned(workspace, 256)) return fail(COLI_EALIGN, "indexer_topk: workspace not 256-byte aligned");
+  if (((steps & 1) && (!aligned(q, 16) || !aligned(keys, 16) || !aligned(w, 4))) ||
+      ((steps & 2) && !aligned(topk_idx, 4)))
+    return fail(COLI_EALIGN, "indexer_topk: q and keys 16-byte, w and topk_idx 4-byte alignment");
+  auto encode = get_encode();
+  if (!encode) return fail(COLI_ECUDA, "indexer_topk: cuTensorMapEncodeTiled is not available");
+  int dev = 0, sms = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce == cudaSuccess) ce = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "indexer_topk: device query");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t off_counts = 256 + align_up((size_t)T * (size_t)L * 4, 256);
+  size_t off = off_counts;
+  int* cand_n = reinterpret_cast<int*>(ws + off);
+  off += align_up((size_t)T * 4, 256);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + off);
+  off += (size_t)T * 65536 * 4;
+  uint32_t* chist = reinterpret_cast<uint32_t*>(ws + off);
+  off += (size_t)T * 2048 * 4;
+  const size_t off_cleared_end = off;
+  uint32_t* sel_bits = reinterpret_cast<uint32_t*>(ws + off);
+  off += align_up((size_t)T * ((L + 31) / 32) * 4, 256);
+  float* cand_val = reinterpret_cast<float*>(ws + off);
+  off += (size_t)T * 2048 * 4;
+  int* cand_idx = reinterpret_cast<int*>(ws + off);
+  if (steps & 1) {
+    ce = cudaMemsetAsync(ws, 0, 64, st);
+    if (ce == cudaSuccess) ce = cudaMemsetAsync(ws + off_counts, 0, off_cleared_end - off_counts, st);
+    if (ce != cudaSuccess) return cuda_fail(ce, "indexer_topk: clear status");
+  }
+  IndexerCall c;
+  c.T = T;
+  c.L = L;
+  c.pos0 = pos0;
+  c.topk = topk;
+  c.q = q;
+  c.w = w;
+  c.keys = keys;
+  c.scores = reinterpret_cast<float*>(ws + 256);
+  c.hist = hist;
+  c.chist = chist;
+  c.sel_bits = sel_bits;
+  c.cand_val = cand_val;
+  c.cand_idx = cand_idx;
+  c.cand_n = cand_n;
+  c.out = topk_idx;
+  c.status = reinterpret_cast<int32_t*>(ws);
+  c.wait_ns = kWaitLimitNs;
+  c.encode = encode;
+  c.steps = steps;
+  ce = launch_indexer(c, st, sms);
+  return ce == cudaSuccess ? COLI_OK : cuda_fail(ce, "indexer_topk: launch");
+}
+
+coli_status colibri_indexer_topk(int T, int L, int pos0, int H, int d, int topk, const void* q, const float* w,
+                                 const void* keys, int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return indexer_call(3, T, L, pos0, H, d, topk, q, w, keys, topk_idx, workspace, workspace_bytes, stream);
+}
+
+coli_status colibri_indexer_scores(int T, int L, int pos0, int H, int d, const void* q, const float* w,
+                                   const void* keys, void* workspace, size_t workspace_bytes, void* stream) {
+  return indexer_call(1, T, L, pos0, H, d, 1, q, w, keys, nullptr, workspace, workspace_bytes, stream);
+}
+
+coli_status colibri_indexer_select(int T, int L, int pos0, int topk, int32_t* topk_idx, void* workspace,
+                                   size_t workspace_bytes, void* stream) {
+  return indexer_call(2, T, L, pos0, 64, 128, topk, nullptr, nullptr, nullptr, topk_idx, workspace,
+                      workspace_bytes, stream);
+}
+
+coli_status colibri_indexer_check_status(const void* workspace, int32_t* device_status, void* stream) {
+  if (!workspace || !device_status) return fail(COLI_EINVAL, "indexer_check_status: null argument");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t ce = cudaMemcpyAsync(&v, workspace, 4, cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "indexer_check_status");
+  *device_status = v;
+  if (v) return fail(COLI_EDEVICE, "indexer device status 0x%x (wait timeout = 2)", v);
+  return COLI_OK;
+}
+
 coli_status colibri_moe_debug_inject(coli_moe_plan_t* plan, int flags, double wait_limit_ms) {
   if (!plan) return fail(COLI_EINVAL, "debug_inject: null plan");
   if (flags & ~(COLI_INJECT_WITHHOLD_STAGE | COLI_INJECT_BAD_EXPERT_ID))

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -141,6 +142,31 @@ cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const vo
 cudaError_t launch_prefill_down(const FwdArgs& a, const void* chunks, const void* tiles, const int32_t* n_tiles,
                                 const CUtensorMap* wmaps, const CUtensorMap& hmap, float* yout, cudaStream_t st,
                                 int num_sms);
+// One call of the sparse-attention key selection (indexer.cu): T query tokens at positions
+// pos0 .. pos0 + T - 1, each with 64 heads of 128 bf16 values (q [T][64][128]) and 64 fp32
+// head weights (w [T][64]); L bf16 keys [L][128]; scores [T][L] fp32 and the selection
+// out [T][topk] int32 (ascending keys, -1 padded) in caller memory.
+struct IndexerCall {
+  int T, L, pos0, topk;
+  const void* q;
+  const float* w;
+  const void* keys;
+  float* scores;
+  uint32_t* hist;        // [T][65536] score histogram (cleared before the scores are computed)
+  uint32_t* chist;       // [T][2048] coarse score histogram (cleared with it)
+  uint32_t* sel_bits;    // [T][ceil(L / 32)] selected-key bitmask
+  float* cand_val;       // [T][2048] boundary-bin keys
+  int* cand_idx;
+  int* cand_n;           // [T] (cleared before the scores are computed)
+  int32_t* out;
+  int32_t* status;
+  unsigned long long wait_ns;
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  int steps;             // 1: scores, 2: selection from the scores, 3: both
+};
+cudaError_t launch_indexer(const IndexerCall& c, cudaStream_t st, int num_sms);
+cudaError_t launch_indexer_scores(const IndexerCall& c, cudaStream_t st, int num_sms);
+
 // int4 decode activations in 16-bit fixed point per block of kXqBlock inputs:
 // x ~= sx * q with sx a power of two (|q| < 2^15), q = 256 * hi + lo with hi a
 // signed and lo an unsigned byte.  Within a block, 64 bytes: 8 words of hi then
