@@ -268,6 +268,73 @@ COLI_API coli_status colibri_moe_profile_begin(coli_moe_plan_t* plan, int max_ca
 COLI_API coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_time* out, int max_kernels, int* n_kernels);
 
 /*
+ * Expert-slot cache in device memory with a host-memory tier.
+ * "25GB RAM runs 744B GLM-5.2" page, section 2: the weights are spread over a
+ * hierarchy of storage tiers and the routed experts a layer needs are read on
+ * demand; section 3.5: a per-layer LRU cache of experts, the next experts read
+ * ahead asynchronously.  "Colibri walkthrough" page, section 3.1: one "expert
+ * slot" holds one expert's weights; a slot keeps last_used and hit_count and
+ * eviction prefers a low hit_count and an old last_used; the engine reports
+ * cache_hit_rate.  Here the lower tier is host memory and the upper tier a
+ * pool of slots in device memory (one cache per layer).
+ *
+ * colibri_moe_cache_slot_bytes: device bytes of one slot (one packed expert).
+ * colibri_moe_cache_create: n_slots slots in caller-owned device memory
+ *   slot_memory (>= n_slots * slot bytes, 256-byte aligned, kept while the
+ *   cache lives); host_experts: HOST array [E] of descriptors whose pointers
+ *   are host memory (pinned memory makes the copies asynchronous and fast)
+ *   holding every routed expert in the layout of coli_qmat; shared: device
+ *   descriptor of the resident shared expert (or NULL).  weight >= 0: the
+ *   eviction weighting -- the victim is the slot, unused by the current
+ *   forward, with the smallest last_used + weight * hit_count (hit_count =
+ *   forwards that used the expert since it entered the slot; 0 = plain LRU;
+ *   ties to the older last_used, then the lower slot).  Allocates the cache's
+ *   small device tables.  Errors: COLI_EINVAL, COLI_EALIGN, COLI_EWORKSPACE,
+ *   COLI_ECUDA.
+ * colibri_moe_forward_cached: the layer forward with weights from the cache.
+ *   After the routing kernels it reads the chosen experts back (it
+ *   synchronises `stream` once), copies each missing expert into a victim slot
+ *   (cudaMemcpyAsync on `stream`) and runs the expert kernels on the slots:
+ *   the output equals colibri_moe_forward's exactly.  Other arguments as
+ *   colibri_moe_forward; COLI_EUNSUPPORTED if the forward needs more distinct
+ *   experts than there are slots.
+ * colibri_moe_cache_prefetch: load the given experts (host array of ids) ahead
+ *   of use on `stream` (e.g. the next layer's predicted experts).  It must not
+ *   run while a forward of the same cache reads the slots on another stream.
+ * colibri_moe_cache_stats / _reset_stats: counters since creation or reset
+ *   (cache_hit_rate = hits / lookups).
+ * colibri_moe_cache_resident: HOST array [E] receives each expert's slot or -1.
+ * colibri_moe_cache_simulate: host only, no GPU: the same policy over a trace
+ *   of n_steps forwards (expert_sets: the distinct ids of each step, set_sizes
+ *   their counts) -> total hits and misses; for choosing n_slots and weight.
+ */
+typedef struct coli_cache coli_cache_t;
+typedef struct {
+  long long forwards;
+  long long lookups;      /* experts the forwards needed */
+  long long hits;
+  long long misses;
+  long long evictions;
+  long long prefetched;   /* experts loaded by colibri_moe_cache_prefetch */
+  long long bytes_copied; /* host -> device */
+} coli_cache_stats;
+COLI_API coli_status colibri_moe_cache_slot_bytes(const coli_moe_plan_t* plan, size_t* bytes);
+COLI_API coli_status colibri_moe_cache_create(coli_moe_plan_t* plan, int n_slots, double weight,
+                                              const coli_expert* host_experts, const coli_expert* shared,
+                                              void* slot_memory, size_t slot_memory_bytes, coli_cache_t** cache);
+COLI_API coli_status colibri_moe_forward_cached(coli_moe_plan_t* plan, coli_cache_t* cache, int T, const void* x,
+                                                const float* router_w, const float* bias, const float* residual,
+                                                float* out, void* workspace, size_t workspace_bytes, void* stream);
+COLI_API coli_status colibri_moe_cache_prefetch(coli_cache_t* cache, const int32_t* experts, int n, void* stream);
+COLI_API coli_status colibri_moe_cache_stats(const coli_cache_t* cache, coli_cache_stats* stats);
+COLI_API coli_status colibri_moe_cache_reset_stats(coli_cache_t* cache);
+COLI_API coli_status colibri_moe_cache_resident(const coli_cache_t* cache, int32_t* slot_of_expert);
+COLI_API void colibri_moe_cache_destroy(coli_cache_t* cache);
+COLI_API coli_status colibri_moe_cache_simulate(int E, int n_slots, double weight, const int32_t* expert_sets,
+                                                const int32_t* set_sizes, int n_steps, int64_t* hits,
+                                                int64_t* misses);
+
+/*
  * Key selection of sparse attention (DSA "lightning indexer" and top-k):
  * "25GB RAM runs 744B GLM-5.2" page, section 3.3: each layer keeps only the
  * top-2048 causal keys for attention; section 4.4: a light indexer scores the

@@ -97,6 +97,25 @@ def lib():
             L.colibri_indexer_select.restype = st
             L.colibri_indexer_check_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int32), vp]
             L.colibri_indexer_check_status.restype = st
+            L.colibri_moe_cache_slot_bytes.argtypes = [vp, ctypes.POINTER(sz)]
+            L.colibri_moe_cache_slot_bytes.restype = st
+            L.colibri_moe_cache_create.argtypes = [vp, i32, ctypes.c_double, ctypes.POINTER(coli_expert),
+                                                   ctypes.POINTER(coli_expert), vp, sz, ctypes.POINTER(vp)]
+            L.colibri_moe_cache_create.restype = st
+            L.colibri_moe_forward_cached.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.colibri_moe_forward_cached.restype = st
+            L.colibri_moe_cache_prefetch.argtypes = [vp, vp, i32, vp]
+            L.colibri_moe_cache_prefetch.restype = st
+            L.colibri_moe_cache_stats.argtypes = [vp, vp]
+            L.colibri_moe_cache_stats.restype = st
+            L.colibri_moe_cache_reset_stats.argtypes = [vp]
+            L.colibri_moe_cache_reset_stats.restype = st
+            L.colibri_moe_cache_resident.argtypes = [vp, vp]
+            L.colibri_moe_cache_resident.restype = st
+            L.colibri_moe_cache_destroy.argtypes = [vp]
+            L.colibri_moe_cache_destroy.restype = None
+            L.colibri_moe_cache_simulate.argtypes = [i32, i32, ctypes.c_double, vp, vp, i32, vp, vp]
+            L.colibri_moe_cache_simulate.restype = st
             L.colibri_moe_last_launch_count.argtypes = [vp]
             L.colibri_moe_last_launch_count.restype = i32
             L.colibri_moe_last_error.argtypes = []
@@ -167,6 +186,79 @@ def colibri_indexer_check_status(workspace, stream=None) -> int:
     if rc not in (COLI_OK, COLI_EDEVICE):
         _check(rc)
     return v.value
+
+
+class coli_cache_stats(ctypes.Structure):
+    _fields_ = [("forwards", ctypes.c_longlong), ("lookups", ctypes.c_longlong), ("hits", ctypes.c_longlong),
+                ("misses", ctypes.c_longlong), ("evictions", ctypes.c_longlong), ("prefetched", ctypes.c_longlong),
+                ("bytes_copied", ctypes.c_longlong)]
+
+
+def colibri_moe_cache_simulate(E: int, n_slots: int, weight: float, expert_sets) -> tuple[int, int]:
+    """(hits, misses) of the expert cache's policy over a trace: expert_sets is a sequence of per-forward
+    collections of distinct expert ids (host only, no GPU)."""
+    sets = [list(map(int, s)) for s in expert_sets]
+    flat = (ctypes.c_int32 * max(1, sum(len(s) for s in sets)))(*[e for s in sets for e in s])
+    sizes = (ctypes.c_int32 * max(1, len(sets)))(*[len(s) for s in sets])
+    h, m = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().colibri_moe_cache_simulate(E, n_slots, weight, flat, sizes, len(sets), ctypes.byref(h),
+                                            ctypes.byref(m)))
+    return h.value, m.value
+
+
+class Cache:
+    """An expert-slot cache of a plan (colibri_moe_cache_create): slots in caller device memory, every routed
+    expert in host memory."""
+
+    def __init__(self, plan, n_slots: int, weight: float, host_experts, slot_memory, slot_memory_bytes: int,
+                 shared=None):
+        arr = (coli_expert * len(host_experts))(*host_experts)
+        sh = ctypes.byref(shared) if shared is not None else None
+        h = ctypes.c_void_p()
+        _check(lib().colibri_moe_cache_create(plan.handle, n_slots, weight, arr, sh, _ptr(slot_memory),
+                                              slot_memory_bytes, ctypes.byref(h)))
+        self.handle = h.value
+        self.plan = plan
+
+    def forward(self, T: int, x, router_w, bias, out, workspace, workspace_bytes: int | None = None, residual=None,
+                stream=None):
+        wb = self.plan.workspace_bytes if workspace_bytes is None else workspace_bytes
+        _check(lib().colibri_moe_forward_cached(self.plan.handle, self.handle, T, _ptr(x), _ptr(router_w), _ptr(bias),
+                                                _ptr(residual), _ptr(out), _ptr(workspace), wb, _stream(stream)))
+
+    def prefetch(self, experts, stream=None):
+        ids = (ctypes.c_int32 * max(1, len(experts)))(*[int(e) for e in experts])
+        _check(lib().colibri_moe_cache_prefetch(self.handle, ids, len(experts), _stream(stream)))
+
+    def stats(self) -> dict:
+        s = coli_cache_stats()
+        _check(lib().colibri_moe_cache_stats(self.handle, ctypes.byref(s)))
+        return {f: getattr(s, f) for f, _ in coli_cache_stats._fields_}
+
+    def reset_stats(self):
+        _check(lib().colibri_moe_cache_reset_stats(self.handle))
+
+    def resident(self, E: int):
+        arr = (ctypes.c_int32 * E)()
+        _check(lib().colibri_moe_cache_resident(self.handle, arr))
+        return list(arr)
+
+    def close(self):
+        if self.handle:
+            lib().colibri_moe_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def colibri_moe_cache_slot_bytes(plan) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().colibri_moe_cache_slot_bytes(plan.handle, ctypes.byref(n)))
+    return n.value
 
 
 def qmat(q, scale, zp) -> coli_qmat:

@@ -10,13 +10,15 @@
 #include <string>
 #include <vector>
 
-#include "moe_internal.cuh"
+#include "plan.h"
 
 using namespace coli;
 
 namespace {
-
 thread_local std::string g_err;
+}  // namespace
+
+namespace coli {
 
 coli_status fail(coli_status s, const char* fmt, ...) {
   char buf[512];
@@ -32,8 +34,9 @@ coli_status cuda_fail(cudaError_t e, const char* what) {
   return fail(COLI_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
-inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+}  // namespace coli
+
+namespace {
 
 enum KernelId {
   K_ROUTE = 0, K_ROUTER, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_GATHER, K_TILES, K_TC_GATEUP, K_TC_DOWN,
@@ -42,6 +45,10 @@ enum KernelId {
 const char* kKernelNames[K_COUNT] = {"route_decode", "router_logits",  "router_topk",    "permute",
                                      "quantize_h",   "expert_gate_up", "expert_down",    "gather_x",
                                      "plan_tiles",   "tc_gate_up",     "tc_down",        "combine"};
+
+}  // namespace
+
+namespace coli {
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -56,29 +63,54 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-}  // namespace
-
-struct coli_moe_plan {
-  coli_moe_desc desc;
-  WsLayout ws;
-  int Fmax;
-  bool bound = false;
-  int device = -1;
-  int num_sms = 0;
-  DevExpert* d_experts = nullptr;
-  CUtensorMap* d_maps = nullptr;
-  // profiling
-  int prof_max_calls = 0;
-  int prof_calls = 0;
-  std::vector<cudaEvent_t> prof_events;  // 2 per kernel launch
-  std::vector<int> prof_kernel;          // kernel id per event pair
-  int last_launches = 0;
-  // failure-path testing (colibri_moe_debug_inject)
-  int inject = 0;
-  unsigned long long wait_ns = kWaitLimitNs;
-};
-
 static int matrix_row_bytes(int qtype, int K) { return qtype == COLI_Q_INT4_G128 ? K / 2 : K; }
+
+coli_status encode_expert(const coli_moe_desc& d, int F, const coli_expert& ex, int id, DevExpert& dx,
+                          CUtensorMap* dec, CUtensorMap* tc) {
+  auto encode = get_encode();
+  if (!encode) return fail(COLI_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const size_t sal = d.qtype == COLI_Q_INT4_G128 ? 2 : 4;
+  const coli_qmat* mats[3] = {&ex.gate, &ex.up, &ex.down};
+  for (int m = 0; m < 3; ++m) {
+    const coli_qmat& qm = *mats[m];
+    if (!qm.q || !qm.scale || !qm.zp) return fail(COLI_EINVAL, "expert %d matrix %d has a null pointer", id, m);
+    if (!aligned(qm.q, 16)) return fail(COLI_EALIGN, "expert %d matrix %d codes not 16-byte aligned", id, m);
+    if (!aligned(qm.scale, sal)) return fail(COLI_EALIGN, "expert %d matrix %d scales misaligned", id, m);
+    const int N = m < 2 ? F : d.d, K = m < 2 ? d.d : F;
+    DevMat& dm = dx.m[m];
+    dm.q = static_cast<const uint8_t*>(qm.q);
+    dm.s = qm.scale;
+    dm.z = static_cast<const uint8_t*>(qm.zp);
+    dm.N = N;
+    dm.K = K;
+    const cuuint64_t row_bytes = (cuuint64_t)matrix_row_bytes(d.qtype, K);
+    const cuuint64_t gdim[2] = {row_bytes, (cuuint64_t)N};
+    const cuuint64_t gstride[1] = {row_bytes};
+    // box width: 256 bytes, or the whole row when rows are shorter (128 bytes)
+    const cuuint32_t boxw = row_bytes < (cuuint64_t)kTmaBoxBytes ? (cuuint32_t)row_bytes : (cuuint32_t)kTmaBoxBytes;
+    const cuuint32_t box[2] = {boxw, (cuuint32_t)(m < 2 ? kGateUpBoxRows : kDownBoxRows)};
+    const cuuint32_t estride[2] = {1, 1};
+    CUresult r = encode(&dec[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim, gstride, box,
+                        estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, id);
+    // tensor-core path: one pipeline stage of codes (32, 64 or 128 bytes) x 128 rows, stored with
+    // the swizzle of the same width so that the dequantising threads read rows without bank conflicts
+    const int pf_row = prefill_raw_row_bytes(d.qtype, m < 2);
+    const cuuint32_t box2[2] = {(cuuint32_t)pf_row, (cuuint32_t)kPrefillRows};
+    const CUtensorMapSwizzle swz = pf_row == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                   : pf_row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                  : CU_TENSOR_MAP_SWIZZLE_128B;
+    r = encode(&tc[m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim, gstride, box2, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "cuTensorMapEncodeTiled (tensor-core box) failed (%d)", (int)r);
+  }
+  dx.F = F;
+  return COLI_OK;
+}
+
+}  // namespace coli
 
 extern "C" {
 
@@ -183,47 +215,11 @@ coli_status colibri_moe_bind_experts(coli_moe_plan_t* plan, const coli_expert* e
   std::vector<CUtensorMap> hm(((size_t)d.E + 1) * 6);   // [0, 3(E+1)): dequant-GEMV boxes; then tensor-core boxes
   memset(hx.data(), 0, hx.size() * sizeof(DevExpert));
   memset(hm.data(), 0, hm.size() * sizeof(CUtensorMap));
-  const size_t sal = d.qtype == COLI_Q_INT4_G128 ? 2 : 4;
   for (int s = 0; s < slots; ++s) {
     const coli_expert& ex = s < d.E ? experts[s] : *shared;
-    const int F = s < d.E ? d.d_ff : d.shared_d_ff;
-    const coli_qmat* mats[3] = {&ex.gate, &ex.up, &ex.down};
-    for (int m = 0; m < 3; ++m) {
-      const coli_qmat& qm = *mats[m];
-      if (!qm.q || !qm.scale || !qm.zp) return fail(COLI_EINVAL, "bind: expert %d matrix %d has a null pointer", s, m);
-      if (!aligned(qm.q, 16)) return fail(COLI_EALIGN, "bind: expert %d matrix %d codes not 16-byte aligned", s, m);
-      if (!aligned(qm.scale, sal)) return fail(COLI_EALIGN, "bind: expert %d matrix %d scales misaligned", s, m);
-      const int N = m < 2 ? F : d.d, K = m < 2 ? d.d : F;
-      DevMat& dm = hx[s].m[m];
-      dm.q = static_cast<const uint8_t*>(qm.q);
-      dm.s = qm.scale;
-      dm.z = static_cast<const uint8_t*>(qm.zp);
-      dm.N = N;
-      dm.K = K;
-      const cuuint64_t row_bytes = (cuuint64_t)matrix_row_bytes(d.qtype, K);
-      const cuuint64_t gdim[2] = {row_bytes, (cuuint64_t)N};
-      const cuuint64_t gstride[1] = {row_bytes};
-      // box width: 256 bytes, or the whole row when rows are shorter (128 bytes)
-      const cuuint32_t boxw = row_bytes < (cuuint64_t)kTmaBoxBytes ? (cuuint32_t)row_bytes : (cuuint32_t)kTmaBoxBytes;
-      const cuuint32_t box[2] = {boxw, (cuuint32_t)(m < 2 ? kGateUpBoxRows : kDownBoxRows)};
-      const cuuint32_t estride[2] = {1, 1};
-      CUresult r = encode(&hm[(size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(qm.q), gdim,
-                          gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled failed (%d) for expert %d", (int)r, s);
-      // tensor-core path: one pipeline stage of codes (32, 64 or 128 bytes) x 128 rows, stored with
-      // the swizzle of the same width so that the dequantising threads read rows without bank conflicts
-      const int pf_row = prefill_raw_row_bytes(d.qtype, m < 2);
-      const cuuint32_t box2[2] = {(cuuint32_t)pf_row, (cuuint32_t)kPrefillRows};
-      const CUtensorMapSwizzle swz = pf_row == 32   ? CU_TENSOR_MAP_SWIZZLE_32B
-                                     : pf_row == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                    : CU_TENSOR_MAP_SWIZZLE_128B;
-      r = encode(&hm[((size_t)d.E + 1) * 3 + (size_t)s * 3 + m], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                 const_cast<void*>(qm.q), gdim, gstride, box2, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "bind: cuTensorMapEncodeTiled (tensor-core box) failed (%d)", (int)r);
-    }
-    hx[s].F = F;
+    const coli_status rc = encode_expert(d, s < d.E ? d.d_ff : d.shared_d_ff, ex, s, hx[s], &hm[(size_t)s * 3],
+                                         &hm[((size_t)d.E + 1) * 3 + (size_t)s * 3]);
+    if (rc != COLI_OK) return rc;
   }
   if (plan->device >= 0 && plan->device != dev)
     return fail(COLI_ESTATE, "bind: plan was bound on device %d, current device is %d", plan->device, dev);
@@ -248,6 +244,16 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
                                 size_t workspace_bytes, void* stream) {
   coli_moe_plan_t* plan = const_cast<coli_moe_plan_t*>(plan_c);
   if (!plan) return fail(COLI_EINVAL, "forward: null plan");
+  const ExpertTables tb{plan->d_experts, plan->d_maps, plan->desc.E, nullptr};
+  return forward_impl(plan, tb, nullptr, nullptr, T, x, router_w, bias, residual, out, workspace, workspace_bytes,
+                      stream);
+}
+
+}  // extern "C"
+
+coli_status coli::forward_impl(coli_moe_plan* plan, const ExpertTables& tb, BetweenFn between, void* ctx, int T,
+                               const void* x, const float* router_w, const float* bias, const float* residual,
+                               float* out, void* workspace, size_t workspace_bytes, void* stream) {
   const coli_moe_desc& d = plan->desc;
   if (!plan->bound) return fail(COLI_ESTATE, "forward: experts not bound (call colibri_moe_bind_experts)");
   if (T < 1 || T > d.T_max) return fail(COLI_EINVAL, "forward: T=%d outside [1, %d]", T, d.T_max);
@@ -264,8 +270,9 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   const WsLayout& w = plan->ws;
   FwdArgs a;
   memset(&a, 0, sizeof(a));
-  a.experts = plan->d_experts;
-  a.maps = plan->d_maps;
+  a.experts = tb.experts;
+  a.maps = tb.maps;
+  a.slot_of = tb.slot_of;
   a.T = T;
   a.d = d.d;
   a.F = d.d_ff;
@@ -339,6 +346,10 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
     if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: permute");
   }
+  if (between) {   // host step between routing and the experts (the expert cache admits the chosen experts)
+    const coli_status rc = between(ctx, a, st);
+    if (rc != COLI_OK) return rc;
+  }
   if (T <= kDecodeMaxT) {
     if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
       return cuda_fail(ce, "forward: expert_gate_up");
@@ -371,7 +382,7 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return fail(COLI_ECUDA, "forward: hidden tensor map (%d)", (int)r);
     }
-    const CUtensorMap* wmaps = plan->d_maps + ((size_t)d.E + 1) * 3;
+    const CUtensorMap* wmaps = tb.maps + ((size_t)tb.n_slots + 1) * 3;
     if ((ce = run(K_GATHER, [&] { return launch_gather_x(a, xh, rows, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: gather_x");
     if ((ce = run(K_TILES, [&] {
@@ -395,6 +406,8 @@ coli_status colibri_moe_forward(const coli_moe_plan_t* plan_c, int T, const void
   if (prof) plan->prof_calls++;
   return COLI_OK;
 }
+
+extern "C" {
 
 coli_status colibri_moe_rmsnorm_bf16(const float* h, int T, int d, float eps, uint16_t* out, void* stream) {
   if (!h || !out) return fail(COLI_EINVAL, "rmsnorm: null pointer");

@@ -47,7 +47,7 @@ constexpr int kMaxNT = 2;                                     // tokens per pass
 static_assert(kGateUpBoxRows == kRows / 2 && kDownBoxRows == kRows, "TMA boxes must match the unit rows");
 
 struct Unit {
-  int slot;   // expert slot (E = shared)
+  int slot;   // storage slot of the expert's weights (its id unless an expert cache maps it)
   int rb;     // row block: gate/up rows rb*8.., down rows rb*16..
   int pbeg;   // first grouped pair row of the expert
   int cnt;    // tokens routed to the expert
@@ -72,8 +72,8 @@ __device__ __forceinline__ bool get_unit(const FwdArgs& a, int u, int n_routed, 
     i = n_routed;
     rb = u - routed_units;
   }
-  const int4 e = __ldcg(a.utab + i);      // (slot, first pair row, pairs), written by the routing kernel
-  out.slot = e.x;
+  const int4 e = __ldcg(a.utab + i);      // (expert, first pair row, pairs), written by the routing kernel
+  out.slot = a.slot_of ? __ldg(a.slot_of + e.x) : e.x;   // where the expert's weights are stored
   out.rb = rb;
   out.pbeg = e.y;
   out.cnt = e.z;

@@ -87,8 +87,9 @@ struct WsLayout {
 
 // Everything a kernel needs to know about one forward call.
 struct FwdArgs {
-  const DevExpert* experts;   // [E+1], slot E = shared
-  const CUtensorMap* maps;    // [(E+1)*3]
+  const DevExpert* experts;   // [n_slots + 1] expert descriptors by storage slot (the last one: shared)
+  const CUtensorMap* maps;    // [(n_slots+1)*3] dequant-GEMV maps, then [(n_slots+1)*3] tensor-core maps
+  const int32_t* slot_of;     // [E+1] storage slot of each expert id (E = shared); NULL: slot = expert id
   int T, d, F, Fs, E, k, qtype, xtype, has_shared;
   float rho;
   int Fmax;                   // row stride of h

@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ntok = ch.ntok;
     mb = tl.mb;
     K = GU ? a.d : (slot == a.E ? a.Fs : a.F);
+    if (a.slot_of) slot = __ldg(a.slot_of + slot);   // where the expert's weights are stored
   };
   auto fail_wait = [&]() {
     set_status(a.status, COLI_DEV_WAIT_TIMEOUT);
