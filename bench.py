@@ -12,6 +12,7 @@ the whole stack; for the indexer one scoring + selection of every query token) o
 Each entry carries its own roofline, end-to-end figure, CPU baseline (the oracle), clock record and
 routing statistics (near-tie tokens, unique experts per step).
 
+  decode + cache    decode T=1 with every expert in pinned host memory behind 32 device slots (weighted LRU)
   indexer T=1 / T=4 sparse-attention key selection: 64 heads of 128, 65,536 cached keys, top-2048
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked|indexer]
@@ -348,10 +349,104 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
         }
         del xs
     cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
+    if name == "decode" and not args.experts and not args.tokens and not args.no_cache:
+        frags["cache"] = bench_cache(dl, layer, w, args, dev, world)
     dl.close()
     del dl, layer
     torch.cuda.empty_cache()
     return frags, cpu, gen_s
+
+
+def bench_cache(dl, layer, w, args, dev, world: int):
+    """Decode at T=1 with the experts in host memory behind a 32-slot device cache (4 x k slots, the
+    walkthrough page's default), router bias Zipf-skewed (as in the prefill workload) so that experts recur.
+    A step is one cached forward: routing, read-back of the chosen experts, copies of the misses from
+    pinned host memory, expert kernels."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import to_dev
+
+    K, W = args.steps, args.warmup
+    T, S, weight = 1, 4 * layer.k, 1.0
+    bias_d = to_dev(H.gen_bias(w.seed, 0, "zipf:0.05:1.1", layer.E), dev)
+    t0 = time.time()
+
+    # the host tier in the slot layout (each expert one contiguous block), so that a miss is one copy
+    sb = coli.colibri_moe_cache_slot_bytes(dl.plan)
+    offs = coli.cache_slot_offsets(layer.d, layer.F, layer.qtype)
+    keep = torch.empty((layer.E, sb), dtype=torch.uint8).pin_memory()
+    kn = keep.numpy()
+    for e in range(layer.E):
+        for j, (n, part) in enumerate((n, p) for n in ("gate", "up", "down") for p in ("q", "s", "z")):
+            src = np.ascontiguousarray(getattr(getattr(layer.experts, n), part)[e]).view(np.uint8).ravel()
+            kn[e, offs[j]:offs[j] + src.size] = src
+    base = keep.data_ptr()
+    host = []
+    for e in range(layer.E):
+        b = base + e * sb
+        q = [coli.qmat(b + offs[3 * m], b + offs[3 * m + 1], b + offs[3 * m + 2]) for m in range(3)]
+        host.append(coli.coli_expert(q[0], q[1], q[2]))
+    pin_s = time.time() - t0
+    slots = torch.empty(S * sb, dtype=torch.uint8, device=dev)
+    cache = coli.Cache(dl.plan, S, weight, host, slots, S * sb)
+    stream = torch.cuda.current_stream(dev)
+    xs = [to_dev(w.x(T, 5000 + i), dev) for i in range(K + W)]
+    out = torch.empty((T, layer.d), dtype=torch.float32, device=dev)
+    ws = torch.empty(dl.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        cache.forward(T, xs[i], dl.router_w, bias_d, out, ws, stream=stream)
+
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize(dev)
+    cache.reset_stats()
+    with ClockSampler(dev.index) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            step(W + i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    st_ = cache.stats()
+    # the same routing trace through the host policy: plain LRU against the weighted rule
+    sets = []
+    for i in range(K + W):
+        dl.plan.forward(T, xs[i], dl.router_w, bias_d, out, dl.ws, stream=stream)
+        sets.append(sorted(set(dl.routing(T)[0].ravel().tolist())))
+
+    def timed_hits(wt):
+        h_all, _ = coli.colibri_moe_cache_simulate(layer.E, S, wt, sets)
+        h_warm, _ = coli.colibri_moe_cache_simulate(layer.E, S, wt, sets[:W])
+        return (h_all - h_warm) / max(1, sum(len(x) for x in sets[W:]))
+
+    hit = st_["hits"] / max(1, st_["lookups"])
+    copy_s = ms * 1e-3
+    cache.close()
+    del keep, slots
+    torch.cuda.empty_cache()
+    return {
+        "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s", "ms_per_step": ms / K,
+        "roofline": {"bound": "hbm", "kernel": "host-to-device expert copies (misses)",
+                     "achieved": st_["bytes_copied"] / copy_s / 1e9, "peak": None, "unit": "GB/s", "frac": None,
+                     "traffic": None, "peak_source": "no measured host-link peak on this pool: copy rate over the "
+                                                     "whole step (routing and kernels included)"},
+        "cache": {"slots": S, "weight": weight, "hit_rate": hit, "lookups": st_["lookups"], "misses": st_["misses"],
+                  "bytes_copied_per_step": st_["bytes_copied"] / K,
+                  "simulated_hit_rate_plain_lru": timed_hits(0.0), "simulated_hit_rate_weighted": timed_hits(weight),
+                  "host_pin_s": round(pin_s, 1)},
+        "e2e": {"value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
+                "h2d_bytes_per_step": st_["bytes_copied"] / K, "d2h_bytes_per_step": 0},
+        "gpu_launches": K * dl.plan.last_launch_count(),
+        "clocks": clk.summary(),
+        "config": {"workload": "decode with an expert cache: GLM-5.2-class MoE layer, T=1 tokens per step, every "
+                               f"expert in pinned host memory, {S} device slots, Zipf-skewed router bias",
+                   "d": layer.d, "d_ff": layer.F, "E": layer.E, "k": layer.k, "qtype": "int4-g128",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 5.86 GB of experts in host memory, misses copied per step"},
+        "cpu_baseline": None,
+    }
 
 
 def bench_stacked(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
@@ -626,7 +721,7 @@ def reference_arm(args, world: int, rank: int):
 
 
 VARIANT_KEYS = ("value", "unit", "ms_per_step", "hbm_gbs_layer", "hbm_frac_layer", "roofline", "kernel_ms_per_step",
-                "e2e", "gpu_launches", "clocks", "routing", "config", "cpu_baseline")
+                "e2e", "gpu_launches", "clocks", "routing", "config", "cpu_baseline", "cache")
 
 
 def main():
@@ -640,6 +735,7 @@ def main():
                     help="all (default): decode T=1 as the headline with decode T=4, MTP verify, prefill and the "
                          "stacked layers as variants; otherwise that workload alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cache", action="store_true", help="skip the expert-cache variant of the decode workload")
     ap.add_argument("--experts", type=int, default=0, help="override E (reduced case for profiler captures)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (reduced case for profiler captures)")
     args = ap.parse_args()
@@ -673,6 +769,9 @@ def main():
         else:
             frags, cpu, gen_s = bench_layer(name, args, dev, world, want_cpu, budget)
             for i, (T, fr) in enumerate(frags.items()):
+                if T == "cache":
+                    results.append(("decode T=1 with expert cache", name, 1, fr))
+                    continue
                 fr["cpu_baseline"] = cpu if i == 0 else None
                 results.append((f"{name} T={T}", name, T, fr))
         gen_total += gen_s

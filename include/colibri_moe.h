@@ -283,7 +283,9 @@ COLI_API coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_
  *   slot_memory (>= n_slots * slot bytes, 256-byte aligned, kept while the
  *   cache lives); host_experts: HOST array [E] of descriptors whose pointers
  *   are host memory (pinned memory makes the copies asynchronous and fast)
- *   holding every routed expert in the layout of coli_qmat; shared: device
+ *   holding every routed expert in the layout of coli_qmat (an expert whose
+ *   nine arrays sit at the offsets of the slot layout -- 256-byte aligned, in
+ *   the order gate q, scale, zp, up ..., down ... -- moves in one copy); shared: device
  *   descriptor of the resident shared expert (or NULL).  weight >= 0: the
  *   eviction weighting -- the victim is the slot, unused by the current
  *   forward, with the smallest last_used + weight * hit_count (hit_count =

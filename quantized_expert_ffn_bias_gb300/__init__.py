@@ -255,6 +255,23 @@ class Cache:
             pass
 
 
+def cache_slot_offsets(d: int, d_ff: int, qtype: int) -> list[int]:
+    """Byte offsets of the nine packed arrays (gate q, scale, zp, up ..., down ...) inside one cache slot,
+    each 256-byte aligned (the layout colibri_moe_cache_slot_bytes sizes); host memory in this layout
+    moves in one copy per miss."""
+    offs, o = [], 0
+    for m in range(3):
+        N, K = (d_ff, d) if m < 2 else (d, d_ff)
+        if qtype == COLI_Q_INT4_G128:
+            parts = (N * K // 2, N * (K // 128) * 2, N * ((K // 128 + 1) // 2))
+        else:
+            parts = (N * K, N * 4, N)
+        for p in parts:
+            offs.append(o)
+            o = (o + p + 255) // 256 * 256
+    return offs
+
+
 def colibri_moe_cache_slot_bytes(plan) -> int:
     n = ctypes.c_size_t()
     _check(lib().colibri_moe_cache_slot_bytes(plan.handle, ctypes.byref(n)))

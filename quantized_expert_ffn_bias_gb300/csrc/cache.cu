@@ -174,6 +174,19 @@ static coli_status copy_expert(coli_cache* c, int e, int slot, cudaStream_t st) 
   const coli_expert& h = c->host[e];
   const coli_qmat* mats[3] = {&h.gate, &h.up, &h.down};
   uint8_t* base = c->slots + (size_t)slot * c->slot_bytes;
+  // an expert stored in host memory in the slot's own layout moves in one copy
+  const uint8_t* h0 = static_cast<const uint8_t*>(h.gate.q);
+  bool packed = true;
+  for (int m = 0; m < 3; ++m) {
+    const void* src[3] = {mats[m]->q, mats[m]->scale, mats[m]->zp};
+    for (int j = 0; j < 3; ++j) packed &= static_cast<const uint8_t*>(src[j]) == h0 + c->off[3 * m + j];
+  }
+  if (packed) {
+    const cudaError_t ce = cudaMemcpyAsync(base, h0, c->slot_bytes, cudaMemcpyHostToDevice, st);
+    if (ce != cudaSuccess) return cuda_fail(ce, "expert cache: copy from host memory");
+    c->stats.bytes_copied += (long long)c->slot_bytes;
+    return COLI_OK;
+  }
   for (int m = 0; m < 3; ++m) {
     const void* src[3] = {mats[m]->q, mats[m]->scale, mats[m]->zp};
     for (int j = 0; j < 3; ++j) {

@@ -93,7 +93,29 @@ def test_cached_forward_equals_resident(torch_cuda, qtype):
     with pytest.raises(coli.ColiError) as e:
         small.forward(2, xd, dl.router_w, dl.bias, torch.empty((2, layer.d), device="cuda"), ws, stream=st)
     assert e.value.status == coli.COLI_EUNSUPPORTED
-    for c in (cache, cache2, small):
+    # host tier packed in the slot layout (one copy per miss)
+    offs = coli.cache_slot_offsets(layer.d, layer.F, qtype)
+    packed = torch.empty((E, sb), dtype=torch.uint8).pin_memory()
+    pn = packed.numpy()
+    for e in range(E):
+        for j, (n, part) in enumerate((n, p) for n in ("gate", "up", "down") for p in ("q", "s", "z")):
+            src = np.ascontiguousarray(getattr(getattr(layer.experts, n), part)[e]).view(np.uint8).ravel()
+            pn[e, offs[j]:offs[j] + src.size] = src
+    hp = []
+    for e in range(E):
+        b = packed.data_ptr() + e * sb
+        q = [coli.qmat(b + offs[3 * m], b + offs[3 * m + 1], b + offs[3 * m + 2]) for m in range(3)]
+        hp.append(coli.coli_expert(q[0], q[1], q[2]))
+    cache3 = coli.Cache(dl.plan, S, 1.0, hp, slots, S * sb, shared=dl.shared.expert(0))
+    for i, T in enumerate([2, 1, 2, 2]):
+        xd = to_dev(H.gen_x(51, 300 + i, T, layer.d, H.X_BF16), "cuda")
+        ref = dl.forward(xd).clone()
+        out = torch.full_like(ref, float("nan"))
+        cache3.forward(T, xd, dl.router_w, dl.bias, out, ws, stream=st)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"packed-tier forward {i} differs from the resident forward"
+    assert cache3.stats()["bytes_copied"] == cache3.stats()["misses"] * sb
+    for c in (cache, cache2, small, cache3):
         c.close()
     dl.close()
-    del keep
+    del keep, packed
