@@ -319,6 +319,7 @@ typedef struct {
   long long evictions;
   long long prefetched;   /* experts loaded by colibri_moe_cache_prefetch */
   long long bytes_copied; /* host -> device */
+  long long predicted;    /* experts named by colibri_moe_cache_pilot */
 } coli_cache_stats;
 COLI_API coli_status colibri_moe_cache_slot_bytes(const coli_moe_plan_t* plan, size_t* bytes);
 COLI_API coli_status colibri_moe_cache_create(coli_moe_plan_t* plan, int n_slots, double weight,
@@ -332,6 +333,23 @@ COLI_API coli_status colibri_moe_cache_stats(const coli_cache_t* cache, coli_cac
 COLI_API coli_status colibri_moe_cache_reset_stats(coli_cache_t* cache);
 COLI_API coli_status colibri_moe_cache_resident(const coli_cache_t* cache, int32_t* slot_of_expert);
 COLI_API void colibri_moe_cache_destroy(coli_cache_t* cache);
+/*
+ * Next-layer routing prediction with read-ahead ("25GB RAM runs 744B GLM-5.2"
+ * page, section 3.5: the experimental PILOT mode predicts the next layer's
+ * routing from the current layer's state and reads those experts ahead).
+ * Runs the next layer's router (plan_next, router_w, bias) on x -- the current
+ * layer's input state, in the next layer's input type -- reads the chosen
+ * experts back (it synchronises `stream` once) and prefetches them into
+ * cache_next on `stream` (up to its slot count).  predicted (HOST int32
+ * [min(E, T*k)], may be NULL) and *n_predicted receive the predicted experts
+ * in ascending order.  workspace: a workspace of plan_next that no running
+ * forward uses.  Use a stream other than the current layer's so that the
+ * copies overlap its compute.  Errors as colibri_moe_forward and
+ * colibri_moe_cache_prefetch.
+ */
+COLI_API coli_status colibri_moe_cache_pilot(coli_moe_plan_t* plan_next, coli_cache_t* cache_next, int T, const void* x,
+                                             const float* router_w, const float* bias, int32_t* predicted,
+                                             int* n_predicted, void* workspace, size_t workspace_bytes, void* stream);
 COLI_API coli_status colibri_moe_cache_simulate(int E, int n_slots, double weight, const int32_t* expert_sets,
                                                 const int32_t* set_sizes, int n_steps, int64_t* hits,
                                                 int64_t* misses);

@@ -114,6 +114,8 @@ def lib():
             L.colibri_moe_cache_resident.restype = st
             L.colibri_moe_cache_destroy.argtypes = [vp]
             L.colibri_moe_cache_destroy.restype = None
+            L.colibri_moe_cache_pilot.argtypes = [vp, vp, i32, vp, vp, vp, vp, ctypes.POINTER(i32), vp, sz, vp]
+            L.colibri_moe_cache_pilot.restype = st
             L.colibri_moe_cache_simulate.argtypes = [i32, i32, ctypes.c_double, vp, vp, i32, vp, vp]
             L.colibri_moe_cache_simulate.restype = st
             L.colibri_moe_last_launch_count.argtypes = [vp]
@@ -191,7 +193,7 @@ def colibri_indexer_check_status(workspace, stream=None) -> int:
 class coli_cache_stats(ctypes.Structure):
     _fields_ = [("forwards", ctypes.c_longlong), ("lookups", ctypes.c_longlong), ("hits", ctypes.c_longlong),
                 ("misses", ctypes.c_longlong), ("evictions", ctypes.c_longlong), ("prefetched", ctypes.c_longlong),
-                ("bytes_copied", ctypes.c_longlong)]
+                ("bytes_copied", ctypes.c_longlong), ("predicted", ctypes.c_longlong)]
 
 
 def colibri_moe_cache_simulate(E: int, n_slots: int, weight: float, expert_sets) -> tuple[int, int]:
@@ -229,6 +231,17 @@ class Cache:
     def prefetch(self, experts, stream=None):
         ids = (ctypes.c_int32 * max(1, len(experts)))(*[int(e) for e in experts])
         _check(lib().colibri_moe_cache_prefetch(self.handle, ids, len(experts), _stream(stream)))
+
+    def pilot(self, T: int, x, router_w, bias, workspace, workspace_bytes: int | None = None, stream=None) -> list:
+        """Predict this cache's layer's experts from x (the previous layer's state) and prefetch them
+        (colibri_moe_cache_pilot); returns the predicted expert ids."""
+        wb = self.plan.workspace_bytes if workspace_bytes is None else workspace_bytes
+        E = self.plan.desc.E
+        buf = (ctypes.c_int32 * E)()
+        n = ctypes.c_int()
+        _check(lib().colibri_moe_cache_pilot(self.plan.handle, self.handle, T, _ptr(x), _ptr(router_w), _ptr(bias),
+                                             buf, ctypes.byref(n), _ptr(workspace), wb, _stream(stream)))
+        return list(buf[:n.value])
 
     def stats(self) -> dict:
         s = coli_cache_stats()

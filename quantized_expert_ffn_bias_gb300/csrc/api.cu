@@ -348,6 +348,10 @@ coli_status coli::forward_impl(coli_moe_plan* plan, const ExpertTables& tb, Betw
   }
   if (between) {   // host step between routing and the experts (the expert cache admits the chosen experts)
     const coli_status rc = between(ctx, a, st);
+    if (rc == kStopAfterRouting) {
+      plan->last_launches = launches;
+      return COLI_OK;
+    }
     if (rc != COLI_OK) return rc;
   }
   if (T <= kDecodeMaxT) {

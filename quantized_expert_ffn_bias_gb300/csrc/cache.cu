@@ -144,6 +144,7 @@ struct coli_cache {
   int32_t* h_unique = nullptr;         // pinned [E + 2]
   coli_cache_stats stats;
   coli_status err = COLI_OK;
+  int pilot_n = 0;                     // experts of the last pilot prediction
 };
 
 static void slot_layout(const coli_moe_desc& d, size_t* off, size_t* len, size_t* total) {
@@ -344,6 +345,38 @@ coli_status colibri_moe_cache_prefetch(coli_cache_t* cache, const int32_t* exper
     const coli_status rc = copy_expert(cache, e, s, st);
     if (rc != COLI_OK) return rc;
   }
+  return COLI_OK;
+}
+
+// Routing-only pass of the next layer: read its chosen experts back and prefetch them.
+static coli_status pilot_between(void* ctx, const FwdArgs& a, cudaStream_t st) {
+  coli_cache* c = static_cast<coli_cache*>(ctx);
+  const int E = a.E;
+  cudaError_t ce = cudaMemcpyAsync(c->h_unique, a.n_unique, 4, cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaMemcpyAsync(c->h_unique + 1, a.unique, (size_t)E * 4, cudaMemcpyDeviceToHost, st);
+  if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
+  if (ce != cudaSuccess) return cuda_fail(ce, "cache_pilot: read the predicted experts");
+  const int nu = c->h_unique[0];
+  if (nu < 0 || nu > E) return fail(COLI_EDEVICE, "cache_pilot: routing reported %d experts", nu);
+  c->pilot_n = nu;
+  const int take = nu < c->pol.n_slots ? nu : c->pol.n_slots;
+  c->stats.predicted += nu;
+  const coli_status rc = colibri_moe_cache_prefetch(c, c->h_unique + 1, take, st);
+  return rc == COLI_OK ? kStopAfterRouting : rc;
+}
+
+coli_status colibri_moe_cache_pilot(coli_moe_plan_t* plan_next, coli_cache_t* cache_next, int T, const void* x,
+                                    const float* router_w, const float* bias, int32_t* predicted, int* n_predicted,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!plan_next || !cache_next) return fail(COLI_EINVAL, "cache_pilot: null argument");
+  if (cache_next->plan != plan_next) return fail(COLI_EINVAL, "cache_pilot: the cache belongs to another plan");
+  const ExpertTables tb{cache_next->d_experts, cache_next->d_maps, cache_next->pol.n_slots, cache_next->d_slot_of};
+  const coli_status rc = forward_impl(plan_next, tb, pilot_between, cache_next, T, x, router_w, bias, nullptr,
+                                      reinterpret_cast<float*>(workspace), workspace, workspace_bytes, stream);
+  if (rc != COLI_OK) return rc;
+  if (n_predicted) *n_predicted = cache_next->pilot_n;
+  if (predicted)
+    for (int i = 0; i < cache_next->pilot_n; ++i) predicted[i] = cache_next->h_unique[1 + i];
   return COLI_OK;
 }
 

@@ -31,8 +31,10 @@ struct ExpertTables {
 };
 
 // Called between the routing kernels and the expert kernels of a forward (after
-// the routing is launched on `st`); returns COLI_OK to go on.
+// the routing is launched on `st`); returns COLI_OK to go on, kStopAfterRouting
+// to end the call there (a routing-only pass), or an error.
 typedef coli_status (*BetweenFn)(void* ctx, const FwdArgs& a, cudaStream_t st);
+constexpr coli_status kStopAfterRouting = static_cast<coli_status>(100);
 
 }  // namespace coli
 
