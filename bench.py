@@ -13,6 +13,7 @@ Each entry carries its own roofline, end-to-end figure, CPU baseline (the oracle
 routing statistics (near-tie tokens, unique experts per step).
 
   decode + cache    decode T=1 with every expert in pinned host memory behind 32 device slots (weighted LRU)
+  decode + pilot    two such layers, layer 1's experts predicted from layer 0's input and read ahead
   indexer T=1 / T=4 sparse-attention key selection: 64 heads of 128, 65,536 cached keys, top-2048
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked|indexer]
@@ -351,10 +352,52 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
     cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
     if name == "decode" and not args.experts and not args.tokens and not args.no_cache:
         frags["cache"] = bench_cache(dl, layer, w, args, dev, world)
+        frags["pilot"] = bench_pilot(dl, layer, w, args, dev, world)
     dl.close()
     del dl, layer
     torch.cuda.empty_cache()
     return frags, cpu, gen_s
+
+
+def _host_tier(dl, layer):
+    """Every routed expert of `layer` in one pinned host buffer, in the slot layout (each expert one
+    contiguous block, so that a miss is one copy).  Returns (buffer, coli_expert per expert, slot bytes)."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    sb = coli.colibri_moe_cache_slot_bytes(dl.plan)
+    offs = coli.cache_slot_offsets(layer.d, layer.F, layer.qtype)
+    keep = torch.empty((layer.E, sb), dtype=torch.uint8).pin_memory()
+    kn = keep.numpy()
+    for e in range(layer.E):
+        for j, (n, part) in enumerate((n, p) for n in ("gate", "up", "down") for p in ("q", "s", "z")):
+            src = np.ascontiguousarray(getattr(getattr(layer.experts, n), part)[e]).view(np.uint8).ravel()
+            kn[e, offs[j]:offs[j] + src.size] = src
+    base = keep.data_ptr()
+    host = []
+    for e in range(layer.E):
+        b = base + e * sb
+        q = [coli.qmat(b + offs[3 * m], b + offs[3 * m + 1], b + offs[3 * m + 2]) for m in range(3)]
+        host.append(coli.coli_expert(q[0], q[1], q[2]))
+    return keep, host, sb
+
+
+def host_link_gbs(sb: int, dev, n: int = 8) -> float:
+    """The host-to-device rate of this GPU's host link: n expert slots (sb bytes each) copied from pinned host
+    memory in one copy, best of 3 (CUDA events).  The denominator of the expert-cache rooflines."""
+    import torch
+    src = torch.empty(n * sb, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(n * sb, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    best = 0.0
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        dst.copy_(src, non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        best = max(best, n * sb / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del src, dst
+    return best
 
 
 def bench_cache(dl, layer, w, args, dev, world: int):
@@ -371,21 +414,7 @@ def bench_cache(dl, layer, w, args, dev, world: int):
     bias_d = to_dev(H.gen_bias(w.seed, 0, "zipf:0.05:1.1", layer.E), dev)
     t0 = time.time()
 
-    # the host tier in the slot layout (each expert one contiguous block), so that a miss is one copy
-    sb = coli.colibri_moe_cache_slot_bytes(dl.plan)
-    offs = coli.cache_slot_offsets(layer.d, layer.F, layer.qtype)
-    keep = torch.empty((layer.E, sb), dtype=torch.uint8).pin_memory()
-    kn = keep.numpy()
-    for e in range(layer.E):
-        for j, (n, part) in enumerate((n, p) for n in ("gate", "up", "down") for p in ("q", "s", "z")):
-            src = np.ascontiguousarray(getattr(getattr(layer.experts, n), part)[e]).view(np.uint8).ravel()
-            kn[e, offs[j]:offs[j] + src.size] = src
-    base = keep.data_ptr()
-    host = []
-    for e in range(layer.E):
-        b = base + e * sb
-        q = [coli.qmat(b + offs[3 * m], b + offs[3 * m + 1], b + offs[3 * m + 2]) for m in range(3)]
-        host.append(coli.coli_expert(q[0], q[1], q[2]))
+    keep, host, sb = _host_tier(dl, layer)
     pin_s = time.time() - t0
     slots = torch.empty(S * sb, dtype=torch.uint8, device=dev)
     cache = coli.Cache(dl.plan, S, weight, host, slots, S * sb)
@@ -423,15 +452,18 @@ def bench_cache(dl, layer, w, args, dev, world: int):
 
     hit = st_["hits"] / max(1, st_["lookups"])
     copy_s = ms * 1e-3
+    link = host_link_gbs(sb, dev)
+    ach = st_["bytes_copied"] / copy_s / 1e9
     cache.close()
     del keep, slots
     torch.cuda.empty_cache()
     return {
         "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s", "ms_per_step": ms / K,
-        "roofline": {"bound": "hbm", "kernel": "host-to-device expert copies (misses)",
-                     "achieved": st_["bytes_copied"] / copy_s / 1e9, "peak": None, "unit": "GB/s", "frac": None,
-                     "traffic": None, "peak_source": "no measured host-link peak on this pool: copy rate over the "
-                                                     "whole step (routing and kernels included)"},
+        "roofline": {"bound": "host link", "kernel": "host-to-device expert copies (misses)",
+                     "achieved": ach, "peak": link, "unit": "GB/s", "frac": ach / link, "traffic": None,
+                     "peak_source": "host-to-device copy of 8 expert slots from pinned memory, measured in this run "
+                                    "(best of 3); achieved = bytes copied over the whole step (routing and kernels "
+                                    "included)"},
         "cache": {"slots": S, "weight": weight, "hit_rate": hit, "lookups": st_["lookups"], "misses": st_["misses"],
                   "bytes_copied_per_step": st_["bytes_copied"] / K,
                   "simulated_hit_rate_plain_lru": timed_hits(0.0), "simulated_hit_rate_weighted": timed_hits(weight),
@@ -445,6 +477,136 @@ def bench_cache(dl, layer, w, args, dev, world: int):
                    "d": layer.d, "d_ff": layer.F, "E": layer.E, "k": layer.k, "qtype": "int4-g128",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2: 5.86 GB of experts in host memory, misses copied per step"},
+        "cpu_baseline": None,
+    }
+
+
+def bench_pilot(dl0, layer0, w, args, dev, world: int):
+    """Two stacked decode layers at T=1 (h <- h + MoE(bf16(RMSNorm(h))); layer 1 generated like layer 0),
+    each with every expert in pinned host memory behind 32 device slots and a Zipf-skewed router bias.
+    With next-layer prediction, layer 1's router runs on layer 0's normalised input on a side stream
+    before layer 0, and the experts it picks are copied into layer 1's cache while layer 0 routes, copies
+    and computes; layer 1 then waits for those copies.  Without it, layer 1 copies its misses after its
+    own routing.  A step is both layers on a fresh input; both modes run the same inputs."""
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import DeviceLayer, to_dev
+
+    K, W = args.steps, args.warmup
+    T, S, d, eps = 1, 4 * layer0.k, w.d, 1e-6
+    t0 = time.time()
+    layer1 = H.gen_layer(w.seed, 1, d=w.d, F=w.F, E=w.E, k=w.k, rho=w.rho, qtype=w.qtypes[0], bias=w.bias,
+                         F_shared=w.F_shared)
+    dl1 = DeviceLayer(layer1, T, device=dev)
+    dls, layers = [dl0, dl1], [layer0, layer1]
+    biases = [to_dev(H.gen_bias(w.seed, l, "zipf:0.05:1.1", w.E), dev) for l in range(2)]
+    tiers = [_host_tier(dls[l], layers[l]) for l in range(2)]
+    gen_s = time.time() - t0
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    xs = [to_dev(w.x(T, 6000 + i), dev) for i in range(K + W)]
+    h, h1, h2 = (torch.empty((T, d), dtype=torch.float32, device=dev) for _ in range(3))
+    n0, n1 = (torch.empty((T, d), dtype=torch.int16, device=dev) for _ in range(2))
+    wss = [torch.empty(dl.plan.workspace_bytes, dtype=torch.uint8, device=dev) for dl in dls]
+    wsp = torch.empty(dl1.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    ev_n, ev_p = torch.cuda.Event(), torch.cuda.Event()
+
+    def run(pilot: bool):
+        sb = tiers[0][2]
+        caches = [coli.Cache(dls[l].plan, S, 1.0, tiers[l][1], torch.empty(S * sb, dtype=torch.uint8, device=dev),
+                             S * sb) for l in range(2)]
+        preds = []
+
+        def step(i):
+            h.copy_(xs[i].view(torch.bfloat16).float())
+            coli.colibri_moe_rmsnorm_bf16(h, T, d, eps, n0, stream)
+            if pilot:
+                ev_n.record(stream)
+                side.wait_event(ev_n)
+                preds.append(caches[1].pilot(T, n0, dl1.router_w, biases[1], wsp, stream=side))
+                ev_p.record(side)
+            caches[0].forward(T, n0, dl0.router_w, biases[0], h1, wss[0], residual=h, stream=stream)
+            coli.colibri_moe_rmsnorm_bf16(h1, T, d, eps, n1, stream)
+            if pilot:
+                stream.wait_event(ev_p)
+            caches[1].forward(T, n1, dl1.router_w, biases[1], h2, wss[1], residual=h1, stream=stream)
+
+        for i in range(W):
+            step(i)
+        torch.cuda.synchronize(dev)
+        for c in caches:
+            c.reset_stats()
+        with ClockSampler(dev.index) as clk:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(K):
+                step(W + i)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        st = [c.stats() for c in caches]
+        launches = dl0.plan.last_launch_count() + dl1.plan.last_launch_count() + 2
+        if pilot:
+            caches[1].pilot(T, n0, dl1.router_w, biases[1], wsp, stream=side)
+            launches += dl1.plan.last_launch_count()
+            torch.cuda.synchronize(dev)
+        for c in caches:
+            c.close()
+        return ms, st, preds[W:], clk.summary(), launches
+
+    ms_p, st_p, preds, clk_p, launches = run(True)
+    ms_n, st_n, _, _, _ = run(False)
+    # recall: layer 1's experts (resident forwards of the same steps) that the prediction named
+    used = named = 0
+    for i in range(K):
+        h.copy_(xs[W + i].view(torch.bfloat16).float())
+        coli.colibri_moe_rmsnorm_bf16(h, T, d, eps, n0, stream)
+        dl0.plan.forward(T, n0, dl0.router_w, biases[0], h1, dl0.ws, dl0.ws.numel(), residual=h, stream=stream)
+        coli.colibri_moe_rmsnorm_bf16(h1, T, d, eps, n1, stream)
+        dl1.plan.forward(T, n1, dl1.router_w, biases[1], h2, dl1.ws, dl1.ws.numel(), stream=stream)
+        torch.cuda.synchronize(dev)
+        act = set(dl1.routing(T)[0].ravel().tolist())
+        used += len(act)
+        named += len(act & set(preds[i]))
+
+    def hit(s):
+        return s["hits"] / max(1, s["lookups"])
+
+    copied = sum(s["bytes_copied"] for s in st_p)
+    link = host_link_gbs(tiers[0][2], dev)
+    ach = copied / (ms_p * 1e-3) / 1e9
+    dl1.close()
+    del tiers, dl1, layer1
+    torch.cuda.empty_cache()
+    return {
+        "value": replica_tokens_per_s(world, K, T, ms_p), "unit": "tokens/s", "ms_per_step": ms_p / K,
+        "roofline": {"bound": "host link", "kernel": "host-to-device expert copies (misses and read-ahead)",
+                     "achieved": ach, "peak": link, "unit": "GB/s", "frac": ach / link, "traffic": None,
+                     "peak_source": "host-to-device copy of 8 expert slots from pinned memory, measured in this run "
+                                    "(best of 3); achieved = bytes copied over the whole step (routing and kernels "
+                                    "included)"},
+        "cache": {"slots_per_layer": S, "weight": 1.0,
+                  "with_prediction": {"ms_per_step": ms_p / K, "hit_rate_layer0": hit(st_p[0]),
+                                      "hit_rate_layer1": hit(st_p[1]),
+                                      "bytes_copied_per_step": copied / K,
+                                      "predicted_per_step": st_p[1]["predicted"] / K,
+                                      "prefetched_per_step": st_p[1]["prefetched"] / K},
+                  "without_prediction": {"ms_per_step": ms_n / K, "hit_rate_layer0": hit(st_n[0]),
+                                         "hit_rate_layer1": hit(st_n[1]),
+                                         "bytes_copied_per_step": sum(s["bytes_copied"] for s in st_n) / K},
+                  "recall_of_layer1_experts": named / max(1, used),
+                  "speedup": ms_n / ms_p,
+                  "host_generation_s": round(gen_s, 1)},
+        "e2e": {"value": replica_tokens_per_s(world, K, T, ms_p), "unit": "tokens/s",
+                "h2d_bytes_per_step": copied / K, "d2h_bytes_per_step": 0},
+        "gpu_launches": K * launches,
+        "clocks": clk_p,
+        "config": {"workload": "decode with expert caches and next-layer prediction: two stacked GLM-5.2-class "
+                               f"MoE layers, T=1 tokens per step, every expert in pinned host memory, {S} device "
+                               "slots per layer, Zipf-skewed router bias",
+                   "d": w.d, "d_ff": w.F, "E": w.E, "k": w.k, "qtype": "int4-g128",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2: 2 x 5.86 GB of experts in host memory, misses copied per step"},
         "cpu_baseline": None,
     }
 
@@ -771,6 +933,9 @@ def main():
             for i, (T, fr) in enumerate(frags.items()):
                 if T == "cache":
                     results.append(("decode T=1 with expert cache", name, 1, fr))
+                    continue
+                if T == "pilot":
+                    results.append(("decode T=1, 2 layers, expert caches + next-layer prediction", name, 1, fr))
                     continue
                 fr["cpu_baseline"] = cpu if i == 0 else None
                 results.append((f"{name} T={T}", name, T, fr))
