@@ -77,6 +77,13 @@ def _bind(L):
                                   ctypes.POINTER(_Expert), vp, i32, vp, vp, i32]
     L.orc_moe_forward.restype = i32
     L.orc_rmsnorm_bf16.argtypes = [i32, vp, f64, vp]
+    if hasattr(L, "orc_mx8_block"):
+        L.orc_mx8_block.argtypes = [i32, vp, f64, vp, vp]
+        L.orc_mx8_block.restype = i32
+        L.orc_expert_ffn_idot.argtypes = [i32, i32, i32, ctypes.POINTER(_Expert), vp, f64, vp, vp, vp]
+        L.orc_moe_forward_idot.argtypes = [ctypes.POINTER(_Desc), vp, vp, vp, ctypes.POINTER(_Expert),
+                                           ctypes.POINTER(_Expert), vp, i32, f64, vp, vp, i32]
+        L.orc_moe_forward_idot.restype = i32
     if hasattr(L, "orc_indexer_scores"):
         L.orc_indexer_scores.argtypes = [i32, i32, i32, i32, i32, vp, vp, vp, vp, i32]
         L.orc_indexer_scores.restype = i32
@@ -191,6 +198,45 @@ class Oracle:
         if rc != 0:
             raise RuntimeError("orc_moe_forward failed")
         return out
+
+
+    def forward_idot(self, x: np.ndarray, tau: float, tokens=None, nthreads: int | None = None):
+        """The layer with integer-dot (IDOT) expert inputs: x and h in blocks of 32 int8 values sharing a
+        power-of-two scale.  Returns (out f64 [n, d], bound f64 [n, d]): bound is the allowance of each output
+        for h values within tau code steps of a rounding boundary (near ties, see orc_mx8_block)."""
+        x = np.ascontiguousarray(x)
+        T = x.shape[0]
+        tokens = np.arange(T, dtype=np.int32) if tokens is None else np.ascontiguousarray(tokens, np.int32)
+        out = np.zeros((len(tokens), self.d), np.float64)
+        bound = np.zeros((len(tokens), self.d), np.float64)
+        rc = self.L.orc_moe_forward_idot(ctypes.byref(self._desc_for(x)), _p(x), _p(self.router_w), _p(self.bias),
+                                        self._experts, self._shared, _p(tokens), len(tokens), float(tau), _p(out),
+                                        _p(bound), nthreads or default_threads())
+        if rc != 0:
+            raise RuntimeError("orc_moe_forward_idot failed")
+        return out, bound
+
+
+def mx8_block(v: np.ndarray, tau: float = 0.0, L=None):
+    """One block of IDOT activations: (vq = q * 2^(e-6) f64 [n], amb f64 [n], e)."""
+    v = np.ascontiguousarray(v, np.float64)
+    vq = np.zeros_like(v)
+    amb = np.zeros_like(v)
+    e = lib(L).orc_mx8_block(len(v), _p(v), float(tau), _p(vq), _p(amb))
+    return vq, amb, e
+
+
+def expert_ffn_idot(bank, e: int, xt: np.ndarray, tau: float = 0.0, L=None):
+    """One token through expert e of `bank` with IDOT inputs: (y f64 [d], ybound f64 [d])."""
+    xt = np.ascontiguousarray(xt, np.float64)
+    d, F = xt.shape[0], bank.F
+    y = np.zeros(d, np.float64)
+    yb = np.zeros(d, np.float64)
+    mx = max(d, F)
+    scratch = np.zeros(2 * mx + 3 * F, np.float64)
+    ex = _Expert(_qmat(bank.gate, e), _qmat(bank.up, e), _qmat(bank.down, e))
+    lib(L).orc_expert_ffn_idot(bank.qtype, d, F, ctypes.byref(ex), _p(xt), float(tau), _p(y), _p(yb), _p(scratch))
+    return y, yb
 
 
 def permute(topk_idx: np.ndarray, E: int, L=None):

@@ -320,3 +320,148 @@ void orc_rmsnorm_bf16(int d, const double* h, double eps, double* n) {
   double r = sqrt(ss / (double)d + eps);
   for (int i = 0; i < d; ++i) n[i] = orc_round_to_bf16(h[i] / r);
 }
+
+/* ---------------------------------------------------------------- integer-dot variant (IDOT) */
+
+/*
+ * "25GB RAM runs 744B GLM-5.2" page (pwwt.cn), section 6 (reproducibility): the
+ * engine has integer-dot kernels (switch IDOT) whose rounding depends on the
+ * batch shape, so their output may differ slightly from the single-token path.
+ * The pages do not give the activation format.  Reading: the inputs of every
+ * quantised matrix-vector product (x for gate and up, h for down) are cut into
+ * blocks of 32 consecutive values; a block shares the scale 2^(e-6) with
+ * e = floor(log2(max |v|)) over the block (e at least -100, so that a block
+ * below 2^-100 becomes zeros), and each value becomes the integer
+ * q = round-half-even(v / 2^(e-6)) clamped to [-127, 127] (an 8-bit integer
+ * with a shared power-of-two exponent, as in the OCP microscaling MXINT8
+ * format).  The weights are unchanged, so every product (c - z) * q is an
+ * integer.  Routing reads x itself.
+ *
+ * orc_mx8_block: n values -> vq = q * 2^(e-6).  With tau > 0, amb[i] bounds
+ * |vq' - vq[i]| for a quantisation of a value within the kernel's rounding
+ * error of v[i] (a near tie): one step 2^(e-6) where |v| / 2^(e-6) lies within
+ * tau of a half-integer, and 1.5 steps for the whole block where max |v| lies
+ * within a relative tau/64 of a power of two (the exponent may differ by one);
+ * zero elsewhere.  Returns e.
+ */
+int orc_mx8_block(int n, const double* v, double tau, double* vq, double* amb) {
+  double m = 0.0;
+  for (int i = 0; i < n; ++i) m = fabs(v[i]) > m ? fabs(v[i]) : m;
+  int e = -100;
+  if (m > 0.0) {
+    int ex;
+    frexp(m, &ex);                  /* m = f * 2^ex, f in [0.5, 1) */
+    e = ex - 1 > -100 ? ex - 1 : -100;
+  }
+  double step = ldexp(1.0, e - 6);
+  int block_amb = 0;
+  if (tau > 0.0 && m > 0.0) {
+    double r = m / ldexp(1.0, e);   /* in [1, 2) unless e was clamped */
+    block_amb = (r - 1.0 < tau / 64.0) || (2.0 - r < tau / 64.0);
+  }
+  for (int i = 0; i < n; ++i) {
+    double s = v[i] / step;         /* exact: a power-of-two scale */
+    double q = nearbyint(s);        /* the default rounding mode: half to even */
+    if (q > 127.0) q = 127.0;
+    if (q < -127.0) q = -127.0;
+    vq[i] = q * step;
+    if (amb) {
+      double a = 0.0;
+      double fr = fabs(s) - floor(fabs(s));
+      if (tau > 0.0 && fabs(fr - 0.5) < tau && fabs(s) < 127.5) a = step;
+      if (block_amb) a = 1.5 * step;
+      amb[i] = a;
+    }
+  }
+  return e;
+}
+
+/*
+ * One token through one SwiGLU expert with IDOT inputs: x -> blocks of 32
+ * (exact decisions: x is read exactly and the scale is a power of two), the
+ * gate/up products and h in double, h -> blocks of 32 with near-tie bounds,
+ * y = Wd hq.  ybound[m] = sum_n |Wd[m][n]| * amb[n].  scratch: at least
+ * 2 * max(d, F) + 3 * F doubles.
+ */
+void orc_expert_ffn_idot(int qtype, int d, int F, const orc_expert* ex, const double* x, double tau, double* y,
+                         double* ybound, double* scratch) {
+  int mx = d > F ? d : F;
+  double* w = scratch;
+  double* xq = scratch + mx;
+  double* h = xq + mx;
+  double* hq = h + F;
+  double* amb = hq + F;
+  for (int b = 0; b < d; b += 32) orc_mx8_block(32, x + b, 0.0, xq + b, NULL);
+  for (int n = 0; n < F; ++n) {
+    double a = 0.0, c = 0.0;
+    orc_dequant_row(&ex->gate, qtype, d, n, w);
+    for (int i = 0; i < d; ++i) a += w[i] * xq[i];
+    orc_dequant_row(&ex->up, qtype, d, n, w);
+    for (int i = 0; i < d; ++i) c += w[i] * xq[i];
+    h[n] = c * silu(a);
+  }
+  for (int b = 0; b < F; b += 32) orc_mx8_block(32, h + b, tau, hq + b, amb + b);
+  for (int m = 0; m < d; ++m) {
+    double acc = 0.0, bnd = 0.0;
+    orc_dequant_row(&ex->down, qtype, F, m, w);
+    for (int n = 0; n < F; ++n) {
+      acc += w[n] * hq[n];
+      bnd += fabs(w[n]) * amb[n];
+    }
+    y[m] = acc;
+    ybound[m] = bnd;
+  }
+}
+
+/*
+ * The layer with IDOT expert products, for a subset of tokens (as
+ * orc_moe_forward): routing on x itself, out[n][d] = sum_j g_j y_j + y_shared
+ * with the IDOT expert outputs, bound[n][d] = sum_j g_j ybound_j + ybound_shared
+ * (the near-tie allowance of each output).  Returns 0, or -1 on allocation
+ * failure.
+ */
+int orc_moe_forward_idot(const orc_desc* D, const void* x, const float* Wr, const float* b, const orc_expert* experts,
+                         const orc_expert* shared, const int32_t* tokens, int n_tok, double tau, double* out,
+                         double* bound, int nthreads) {
+  int d = D->d, E = D->E, k = D->k, F = D->F;
+  int Fmax = F > D->F_shared ? F : D->F_shared;
+  int mx = d > Fmax ? d : Fmax;
+  int bad = 0;
+#pragma omp parallel num_threads(nthreads > 0 ? nthreads : 1)
+  {
+    double* xt = (double*)malloc(sizeof(double) * (size_t)d);
+    double* y = (double*)malloc(sizeof(double) * (size_t)d);
+    double* yb = (double*)malloc(sizeof(double) * (size_t)d);
+    double* scratch = (double*)malloc(sizeof(double) * (2 * (size_t)mx + 3 * (size_t)Fmax));
+    double* s = (double*)malloc(sizeof(double) * (size_t)E);
+    double* u = (double*)malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    int32_t* sel = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+    double* g = (double*)malloc(sizeof(double) * (size_t)k);
+    if (!xt || !y || !yb || !scratch || !s || !u || !taken || !sel || !g) {
+#pragma omp atomic write
+      bad = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int n = 0; n < n_tok; ++n) {
+        int t = tokens[n];
+        double gap;
+        for (int i = 0; i < d; ++i) xt[i] = x_at(D->xtype, x, (size_t)t * (size_t)d + (size_t)i);
+        route_token(d, E, k, D->rho, xt, Wr, b, sel, g, &gap, s, u, taken);
+        double* o = out + (size_t)n * (size_t)d;
+        double* ob = bound + (size_t)n * (size_t)d;
+        for (int i = 0; i < d; ++i) { o[i] = 0.0; ob[i] = 0.0; }
+        for (int j = 0; j < k; ++j) {
+          orc_expert_ffn_idot(D->qtype, d, F, &experts[sel[j]], xt, tau, y, yb, scratch);
+          for (int i = 0; i < d; ++i) { o[i] += g[j] * y[i]; ob[i] += g[j] * yb[i]; }
+        }
+        if (D->has_shared && shared) {
+          orc_expert_ffn_idot(D->qtype_shared, d, D->F_shared, shared, xt, tau, y, yb, scratch);
+          for (int i = 0; i < d; ++i) { o[i] += y[i]; ob[i] += yb[i]; }
+        }
+      }
+    }
+    free(xt); free(y); free(yb); free(scratch); free(s); free(u); free(taken); free(sel); free(g);
+  }
+  return bad ? -1 : 0;
+}

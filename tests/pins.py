@@ -480,4 +480,159 @@ def pin_stacked_selection_layers(L=None):
     assert np.allclose(h, hh, rtol=1e-12, atol=1e-14)
 
 
+# ----------------------------------------------------------------------------- integer-dot (IDOT) inputs
+
+
+def mx8_brute(v):
+    """Brute force of the IDOT block rule: e by integer search (2^e <= max|v| < 2^(e+1), e >= -100), then for
+    each value the code among all of -127..127 nearest to v / 2^(e-6), a tie going to the even code."""
+    v = np.asarray(v, np.float64)
+    m = float(np.abs(v).max())
+    e = -100
+    if m > 0.0:
+        e = 0
+        while 2.0 ** e > m:
+            e -= 1
+        while 2.0 ** (e + 1) <= m:
+            e += 1
+        e = max(e, -100)
+    step = 2.0 ** (e - 6)
+    codes = np.arange(-127, 128, dtype=np.float64)
+    out = np.empty_like(v)
+    for i, x in enumerate(v):
+        dist = np.abs(codes * step - x)
+        best = np.flatnonzero(dist == dist.min())
+        pick = best[0] if len(best) == 1 else [b for b in best if int(codes[b]) % 2 == 0][0]
+        out[i] = codes[pick] * step
+    return out, e
+
+
+def pin_mx8_closed_forms(L=None):
+    # max |v| = 1: the step is 2^-6 and multiples of it are kept exactly
+    v = np.array([1.0] + [k / 64.0 for k in range(-31, 31)][:31])
+    vq, amb, e = O.mx8_block(v, L=L)
+    assert e == 0 and np.array_equal(vq, v)
+    # half steps go to the even code; negative values mirror positive ones
+    v = np.array([1.0, 0.5 / 64, 1.5 / 64, 2.5 / 64, -2.5 / 64, -0.5 / 64, 126.5 / 64] + [0.0] * 25)
+    vq, _, e = O.mx8_block(v, L=L)
+    assert e == 0
+    assert np.array_equal(vq[:7], np.array([64, 0, 2, 2, -2, 0, 126]) / 64.0)
+    # codes saturate at +-127: 1.999 / 2^-6 rounds to 128
+    vq, _, e = O.mx8_block(np.array([1.999, -1.999] + [0.25] * 30), L=L)
+    assert e == 0 and vq[0] == 127 / 64.0 and vq[1] == -127 / 64.0 and vq[2] == 0.25
+    # zeros, and blocks below 2^-100, become zeros
+    vq, _, e = O.mx8_block(np.zeros(32), L=L)
+    assert e == -100 and not vq.any()
+    vq, _, e = O.mx8_block(np.full(32, 2.0 ** -110), L=L)
+    assert e == -100 and not vq.any()
+    # scaling the block by 2^j scales the result by 2^j
+    rng = np.random.default_rng(21)
+    v = rng.standard_normal(32)
+    base, _, e0 = O.mx8_block(v, L=L)
+    for j in (-9, -1, 1, 13):
+        vq, _, e = O.mx8_block(v * 2.0 ** j, L=L)
+        assert e == e0 + j and np.array_equal(vq, base * 2.0 ** j)
+
+
+def pin_mx8_brute_force(L=None):
+    """Random blocks (several magnitudes, exact ties and saturating maxima planted) against brute force; the
+    error of every value is at most half a step, or one step where the code saturated."""
+    rng = np.random.default_rng(22)
+    for trial in range(120):
+        scale = 2.0 ** rng.integers(-30, 30)
+        v = rng.standard_normal(32) * scale
+        if trial % 3 == 1:      # plant exact half steps
+            m = float(np.abs(v).max())
+            e = int(np.floor(np.log2(m)))
+            st = 2.0 ** (e - 6)
+            v[1:6] = (rng.integers(-120, 120, 5) + 0.5) * st
+        if trial % 5 == 2:      # plant a maximum that saturates
+            m = float(np.abs(v).max())
+            e = int(np.floor(np.log2(m)))
+            v[0] = 1.995 * 2.0 ** e
+            v[1:] = np.clip(v[1:], -1.9 * 2.0 ** e, 1.9 * 2.0 ** e)
+        vq, _, e = O.mx8_block(v, L=L)
+        want, we = mx8_brute(v)
+        assert e == we and np.array_equal(vq, want), trial
+        st = 2.0 ** (e - 6)
+        err = np.abs(vq - v)
+        sat = np.abs(v) / st >= 127.5
+        assert np.all(err[~sat] <= st / 2) and np.all(err[sat] <= st)
+
+
+def pin_mx8_near_tie_allowance(L=None):
+    """tau marks values within tau code steps of a half step (one step) and whole blocks whose maximum is
+    within a relative tau/64 of a power of two (1.5 steps); nothing else."""
+    st = 2.0 ** -6
+    v = np.array([1.5, 3.5 * st, (3.5 + 0.01) * st, (10.5 - 0.004) * st, 0.3 * st, 7.0 * st] + [0.0] * 26)
+    _, amb, e = O.mx8_block(v, tau=0.005, L=L)
+    assert e == 0
+    assert np.array_equal(amb[:6], np.array([0.0, st, 0.0, st, 0.0, 0.0])) and not amb[6:].any()
+    # maximum exactly a power of two: the kernel's value may sit just below it (exponent one less)
+    _, amb, _ = O.mx8_block(np.array([1.0, 0.3, -0.2] + [0.0] * 29), tau=0.005, L=L)
+    assert np.all(amb == 1.5 * st)
+    # maximum just under the next power of two
+    _, amb, _ = O.mx8_block(np.array([2.0 * (1 - 1e-6), 0.3] + [0.0] * 30), tau=0.005, L=L)
+    assert np.all(amb == 1.5 * st)
+    # tau = 0: no allowance anywhere
+    _, amb, _ = O.mx8_block(np.array([1.0, 3.5 * st] + [0.0] * 30), tau=0.0, L=L)
+    assert not amb.any()
+
+
+def pin_idot_expert_brute_force(L=None):
+    """An IDOT expert against numpy matmuls on numpy-dequantised weights with brute-force block
+    quantisation of x and of h; the near-tie bound against its definition."""
+    rng = np.random.default_rng(23)
+    for qt, d, F in ((H.Q_INT4_G128, 256, 128), (H.Q_INT8_PC, 256, 192)):
+        layer = tiny_layer(qtype=qt, E=3, d=d, F=F)
+        Wg, Wu, Wd = (dense_dequant(m) for m in (layer.experts.gate, layer.experts.up, layer.experts.down))
+        for e in range(3):
+            xt = x_as_f64(H.to_bf16_bits(rng.standard_normal(d).astype(np.float32)))
+            tau = 0.01
+            y, yb = O.expert_ffn_idot(layer.experts, e, xt, tau, L=L)
+            xq = np.concatenate([mx8_brute(xt[b:b + 32])[0] for b in range(0, d, 32)])
+            h = silu(Wg[e] @ xq) * (Wu[e] @ xq)
+            hq, amb = [], []
+            for b in range(0, F, 32):
+                q, eb = mx8_brute(h[b:b + 32])
+                hq.append(q)
+                st = 2.0 ** (eb - 6)
+                s = np.abs(h[b:b + 32]) / st
+                a = np.where((np.abs(s - np.floor(s) - 0.5) < tau) & (s < 127.5), st, 0.0)
+                r = np.abs(h[b:b + 32]).max() / 2.0 ** eb
+                if r - 1 < tau / 64 or 2 - r < tau / 64:
+                    a[:] = 1.5 * st
+                amb.append(a)
+            hq, amb = np.concatenate(hq), np.concatenate(amb)
+            assert np.allclose(y, Wd[e] @ hq, rtol=1e-11, atol=1e-13), (qt, e)
+            assert np.allclose(yb, np.abs(Wd[e]) @ amb, rtol=1e-11, atol=1e-15), (qt, e)
+
+
+def pin_idot_layer_combination(L=None):
+    """The IDOT layer = routing of x itself (the exact layer's selection and gate weights) times the IDOT
+    experts, plus the shared expert with weight 1; the bound combines with the same weights; and the IDOT
+    layer stays within its quantisation error of the exact layer."""
+    for qt in (H.Q_INT8_PC, H.Q_INT4_G128):
+        layer = tiny_layer(qtype=qt, k=3, F_shared=128)
+        x = H.gen_x(0, 4, 6, layer.d, H.X_BF16)
+        orc = O.Oracle(layer, L)
+        idx, w, gap, s = orc.route(x)
+        out, bound = orc.forward_idot(x, 0.01)
+        exact = orc.forward(x)
+        xf = x_as_f64(x)
+        for t in range(6):
+            want = np.zeros(layer.d)
+            wb = np.zeros(layer.d)
+            for j in range(layer.k):
+                y, yb = O.expert_ffn_idot(layer.experts, int(idx[t, j]), xf[t], 0.01, L=L)
+                want += w[t, j] * y
+                wb += w[t, j] * yb
+            y, yb = O.expert_ffn_idot(layer.shared, 0, xf[t], 0.01, L=L)
+            assert np.allclose(out[t], want + y, rtol=1e-12, atol=1e-14), (qt, t)
+            assert np.allclose(bound[t], wb + yb, rtol=1e-12, atol=1e-16), (qt, t)
+        # 8-bit inputs: a few per cent of the output's spread at most
+        rel = np.abs(out - exact).max() / np.abs(exact).max()
+        assert 1e-5 < rel < 0.05, (qt, rel)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -42,6 +42,20 @@ MUTANTS = {
     "bf16_truncates": ("return nearbyint(v / quantum) * quantum;", "return trunc(v / quantum) * quantum;"),
     "logit_drops_last_input": ("for (int i = 0; i < d; ++i) z += xt[i] * (double)we[i];",
                                "for (int i = 0; i < d - 1; ++i) z += xt[i] * (double)we[i];"),
+    "mx8_exponent_high": ("e = ex - 1 > -100 ? ex - 1 : -100;", "e = ex > -100 ? ex : -100;"),
+    "mx8_clamp_128": ("if (q > 127.0) q = 127.0;", "if (q > 128.0) q = 128.0;"),
+    "mx8_ties_away": ("double q = nearbyint(s);        /* the default rounding mode: half to even */",
+                      "double q = round(s);"),
+    "mx8_truncates": ("double q = nearbyint(s);        /* the default rounding mode: half to even */",
+                      "double q = trunc(s);"),
+    "idot_x_unquantised": ("for (int i = 0; i < d; ++i) a += w[i] * xq[i];",
+                           "for (int i = 0; i < d; ++i) a += w[i] * x[i];"),
+    "idot_h_unquantised": ("acc += w[n] * hq[n];", "acc += w[n] * h[n];"),
+    "idot_bound_signed": ("bnd += fabs(w[n]) * amb[n];", "bnd += w[n] * amb[n];"),
+    "idot_block_tie_one_side": ("block_amb = (r - 1.0 < tau / 64.0) || (2.0 - r < tau / 64.0);",
+                                "block_amb = (r - 1.0 < tau / 64.0);"),
+    "idot_shared_bound_dropped": ("for (int i = 0; i < d; ++i) { o[i] += y[i]; ob[i] += yb[i]; }",
+                                  "for (int i = 0; i < d; ++i) { o[i] += y[i]; }"),
 }
 
 
