@@ -246,6 +246,38 @@ COLI_API coli_status colibri_moe_check_status(const coli_moe_plan_t* plan, const
  * meaningful; the next forward without injection is a normal one.
  * Errors: COLI_EINVAL (null plan or unknown flag bits).
  */
+/*
+ * Integer-dot expert inputs (the IDOT switch of the "25GB RAM runs 744B
+ * GLM-5.2" page, section 6 (reproducibility): integer kernels whose rounding
+ * depends on the batch shape, so that their output may differ slightly from
+ * the single-token path).  enable = 1: the inputs of the expert matrices (x for
+ * gate and up, the SwiGLU output h for down) are cut into blocks of 32 values
+ * that share the scale 2^(e-6), e = floor(log2(max |v|)) over the block (at
+ * least -100), and each value becomes the int8 code round-half-even(v / 2^(e-6))
+ * clamped to [-127, 127].  Up to 8 tokens per call the expert kernels take
+ * integer dot products of the weight codes with these codes; above that the
+ * tensor-core kernels take the values code * 2^(e-6) as fp16 operands, which is
+ * exact for 2^-18 <= max |v| < 2^16 per block.  Routing always reads x itself.
+ * enable = 0 (the default) restores the default inputs.  Takes effect at the
+ * next forward call.  Errors: COLI_EINVAL (null plan, enable not 0 or 1).
+ */
+COLI_API coli_status colibri_moe_set_idot(coli_moe_plan_t* plan, int enable);
+
+/*
+ * Test and debugging aid: the input of the down projection in the last
+ * forward call on `workspace` (made with T tokens and the plan's current IDOT
+ * setting), as the down kernels read it (the SwiGLU output h of the "Colibri
+ * walkthrough" page, section 3.4, after the kernels' own conversion: 16-bit
+ * fixed point, integer-dot codes times their block scale, or fp16).
+ * h_out: DEVICE memory, [T*k + (has_shared ? T : 0)][max(d_ff, shared_d_ff)]
+ * floats; rows in the grouped order of colibri_moe_debug_routing's pair_token
+ * and pair_slot, then the shared expert's rows (token order); columns past the
+ * row's expert's FFN size are 0.  Asynchronous on `stream`.
+ * Errors: COLI_EINVAL (null argument, bad T), COLI_EALIGN, COLI_ECUDA.
+ */
+COLI_API coli_status colibri_moe_debug_hidden(const coli_moe_plan_t* plan, const void* workspace, int T,
+                                              float* h_out, void* stream);
+
 #define COLI_INJECT_WITHHOLD_STAGE 1
 #define COLI_INJECT_BAD_EXPERT_ID 2
 COLI_API coli_status colibri_moe_debug_inject(coli_moe_plan_t* plan, int flags, double wait_limit_ms);

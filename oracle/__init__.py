@@ -81,6 +81,7 @@ def _bind(L):
         L.orc_mx8_block.argtypes = [i32, vp, f64, vp, vp]
         L.orc_mx8_block.restype = i32
         L.orc_expert_ffn_idot.argtypes = [i32, i32, i32, ctypes.POINTER(_Expert), vp, f64, vp, vp, vp]
+        L.orc_idot_hidden.argtypes = [i32, i32, i32, ctypes.POINTER(_Expert), vp, f64, vp, vp, vp, vp]
         L.orc_moe_forward_idot.argtypes = [ctypes.POINTER(_Desc), vp, vp, vp, ctypes.POINTER(_Expert),
                                            ctypes.POINTER(_Expert), vp, i32, f64, vp, vp, i32]
         L.orc_moe_forward_idot.restype = i32
@@ -237,6 +238,19 @@ def expert_ffn_idot(bank, e: int, xt: np.ndarray, tau: float = 0.0, L=None):
     ex = _Expert(_qmat(bank.gate, e), _qmat(bank.up, e), _qmat(bank.down, e))
     lib(L).orc_expert_ffn_idot(bank.qtype, d, F, ctypes.byref(ex), _p(xt), float(tau), _p(y), _p(yb), _p(scratch))
     return y, yb
+
+
+def idot_hidden(bank, e: int, xt: np.ndarray, tau: float = 0.0, L=None):
+    """The down projection's input of one token in expert e with IDOT inputs: (h f64 [F], hq f64 [F] (the
+    values q * 2^(e-6)), amb f64 [F] (near-tie bounds))."""
+    xt = np.ascontiguousarray(xt, np.float64)
+    d, F = xt.shape[0], bank.F
+    h, hq, amb = (np.zeros(F, np.float64) for _ in range(3))
+    scratch = np.zeros(2 * max(d, F), np.float64)
+    ex = _Expert(_qmat(bank.gate, e), _qmat(bank.up, e), _qmat(bank.down, e))
+    lib(L).orc_idot_hidden(bank.qtype, d, F, ctypes.byref(ex), _p(xt), float(tau), _p(h), _p(hq), _p(amb),
+                           _p(scratch))
+    return h, hq, amb
 
 
 def permute(topk_idx: np.ndarray, E: int, L=None):

@@ -330,8 +330,9 @@ void orc_rmsnorm_bf16(int d, const double* h, double eps, double* n) {
  * The pages do not give the activation format.  Reading: the inputs of every
  * quantised matrix-vector product (x for gate and up, h for down) are cut into
  * blocks of 32 consecutive values; a block shares the scale 2^(e-6) with
- * e = floor(log2(max |v|)) over the block (e at least -100, so that a block
- * below 2^-100 becomes zeros), and each value becomes the integer
+ * e = floor(log2(max |v|)) over the block (e at least -100, so that the scale
+ * stays a normal single-precision number; an all-zero block has e = -100), and
+ * each value becomes the integer
  * q = round-half-even(v / 2^(e-6)) clamped to [-127, 127] (an 8-bit integer
  * with a shared power-of-two exponent, as in the OCP microscaling MXINT8
  * format).  The weights are unchanged, so every product (c - z) * q is an
@@ -377,20 +378,17 @@ int orc_mx8_block(int n, const double* v, double tau, double* vq, double* amb) {
 }
 
 /*
- * One token through one SwiGLU expert with IDOT inputs: x -> blocks of 32
- * (exact decisions: x is read exactly and the scale is a power of two), the
- * gate/up products and h in double, h -> blocks of 32 with near-tie bounds,
- * y = Wd hq.  ybound[m] = sum_n |Wd[m][n]| * amb[n].  scratch: at least
- * 2 * max(d, F) + 3 * F doubles.
+ * The down projection's input of one token in one expert with IDOT inputs:
+ * x -> blocks of 32 (exact decisions: x is read exactly and the scale is a
+ * power of two), the gate/up products and h[F] in double, then h -> blocks of
+ * 32: hq[F] (the values q * 2^(e-6)) and amb[F] (near-tie bounds, tau as in
+ * orc_mx8_block).  scratch: at least 2 * max(d, F) doubles.
  */
-void orc_expert_ffn_idot(int qtype, int d, int F, const orc_expert* ex, const double* x, double tau, double* y,
-                         double* ybound, double* scratch) {
+void orc_idot_hidden(int qtype, int d, int F, const orc_expert* ex, const double* x, double tau, double* h,
+                     double* hq, double* amb, double* scratch) {
   int mx = d > F ? d : F;
   double* w = scratch;
   double* xq = scratch + mx;
-  double* h = xq + mx;
-  double* hq = h + F;
-  double* amb = hq + F;
   for (int b = 0; b < d; b += 32) orc_mx8_block(32, x + b, 0.0, xq + b, NULL);
   for (int n = 0; n < F; ++n) {
     double a = 0.0, c = 0.0;
@@ -401,6 +399,21 @@ void orc_expert_ffn_idot(int qtype, int d, int F, const orc_expert* ex, const do
     h[n] = c * silu(a);
   }
   for (int b = 0; b < F; b += 32) orc_mx8_block(32, h + b, tau, hq + b, amb + b);
+}
+
+/*
+ * One token through one SwiGLU expert with IDOT inputs: orc_idot_hidden, then
+ * y = Wd hq and ybound[m] = sum_n |Wd[m][n]| * amb[n].  scratch: at least
+ * 2 * max(d, F) + 3 * F doubles.
+ */
+void orc_expert_ffn_idot(int qtype, int d, int F, const orc_expert* ex, const double* x, double tau, double* y,
+                         double* ybound, double* scratch) {
+  int mx = d > F ? d : F;
+  double* w = scratch;
+  double* h = scratch + 2 * (size_t)mx;
+  double* hq = h + F;
+  double* amb = hq + F;
+  orc_idot_hidden(qtype, d, F, ex, x, tau, h, hq, amb, scratch);
   for (int m = 0; m < d; ++m) {
     double acc = 0.0, bnd = 0.0;
     orc_dequant_row(&ex->down, qtype, F, m, w);

@@ -87,6 +87,10 @@ def lib():
             L.colibri_moe_profile_end.restype = st
             L.colibri_moe_debug_inject.argtypes = [vp, i32, ctypes.c_double]
             L.colibri_moe_debug_inject.restype = st
+            L.colibri_moe_set_idot.argtypes = [vp, i32]
+            L.colibri_moe_debug_hidden.argtypes = [vp, vp, i32, vp, vp]
+            L.colibri_moe_debug_hidden.restype = st
+            L.colibri_moe_set_idot.restype = st
             L.colibri_indexer_workspace_size.argtypes = [i32, i32, ctypes.POINTER(sz)]
             L.colibri_indexer_workspace_size.restype = st
             L.colibri_indexer_topk.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, sz, vp]
@@ -367,6 +371,18 @@ class Plan:
         _check(lib().colibri_moe_debug_inject(self.handle, flags, wait_limit_ms))
 
     debug_inject = colibri_moe_debug_inject
+
+    def colibri_moe_set_idot(self, enable: bool):
+        """Integer-dot expert inputs (int8 codes per block of 32 with a power-of-two scale) on or off."""
+        _check(lib().colibri_moe_set_idot(self.handle, 1 if enable else 0))
+
+    set_idot = colibri_moe_set_idot
+
+    def colibri_moe_debug_hidden(self, workspace, T: int, h_out, stream=None):
+        """The down projection's input of the last forward (device float [rows, Fmax], grouped row order)."""
+        _check(lib().colibri_moe_debug_hidden(self.handle, _ptr(workspace), T, _ptr(h_out), _stream(stream)))
+
+    debug_hidden = colibri_moe_debug_hidden
 
     def colibri_moe_last_launch_count(self) -> int:
         return lib().colibri_moe_last_launch_count(self.handle)

@@ -312,6 +312,7 @@ coli_status coli::forward_impl(coli_moe_plan* plan, const ExpertTables& tb, Betw
   a.y = reinterpret_cast<float*>(ws + w.y);
   a.wait_ns = plan->wait_ns;
   a.inject = plan->inject;
+  a.idot = plan->idot;
 
   const bool prof = plan->prof_calls < plan->prof_max_calls;
   int launches = 0;
@@ -357,7 +358,7 @@ coli_status coli::forward_impl(coli_moe_plan* plan, const ExpertTables& tb, Betw
   if (T <= kDecodeMaxT) {
     if ((ce = run(K_GATEUP, [&] { return launch_decode_gateup(a, T, st, plan->num_sms); })) != cudaSuccess)
       return cuda_fail(ce, "forward: expert_gate_up");
-    if (d.qtype == COLI_Q_INT4_G128 &&
+    if ((d.qtype == COLI_Q_INT4_G128 || a.idot) &&
         (ce = run(K_PREP, [&] { return launch_quantize_h(a, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: quantize_h");
     if ((ce = run(K_DOWN, [&] { return launch_decode_down(a, T, st, plan->num_sms); })) != cudaSuccess)
@@ -607,6 +608,42 @@ coli_status colibri_indexer_check_status(const void* workspace, int32_t* device_
   if (ce != cudaSuccess) return cuda_fail(ce, "indexer_check_status");
   *device_status = v;
   if (v) return fail(COLI_EDEVICE, "indexer device status 0x%x (wait timeout = 2)", v);
+  return COLI_OK;
+}
+
+coli_status colibri_moe_debug_hidden(const coli_moe_plan_t* plan, const void* workspace, int T, float* h_out,
+                                     void* stream) {
+  if (!plan || !workspace || !h_out) return fail(COLI_EINVAL, "debug_hidden: null argument");
+  if (T < 1 || T > plan->desc.T_max) return fail(COLI_EINVAL, "debug_hidden: bad T");
+  if (!aligned(h_out, 4)) return fail(COLI_EALIGN, "debug_hidden: h_out must be 4-byte aligned");
+  const coli_moe_desc& d = plan->desc;
+  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+  const WsLayout& w = plan->ws;
+  HiddenView v;
+  const bool i4 = d.qtype == COLI_Q_INT4_G128;
+  if (T > kDecodeMaxT) v.mode = 4;
+  else if (plan->idot) v.mode = i4 ? 2 : 3;
+  else v.mode = i4 ? 0 : 1;
+  v.perm = i4 ? 1 : 0;
+  v.qtype = d.qtype;
+  v.P = T * d.k;
+  v.rows = v.P + (d.has_shared ? T : 0);
+  v.F = d.d_ff;
+  v.Fs = d.has_shared ? d.shared_d_ff : 0;
+  v.Fmax = plan->Fmax;
+  v.h = reinterpret_cast<const float*>(ws + w.h);
+  v.hq = ws + w.hq;
+  v.hqs = reinterpret_cast<const int2*>(ws + w.hqs);
+  v.hh = reinterpret_cast<const __half*>(ws + w.h);
+  v.out = h_out;
+  const cudaError_t ce = launch_debug_hidden(v, static_cast<cudaStream_t>(stream));
+  return ce == cudaSuccess ? COLI_OK : cuda_fail(ce, "debug_hidden");
+}
+
+coli_status colibri_moe_set_idot(coli_moe_plan_t* plan, int enable) {
+  if (!plan) return fail(COLI_EINVAL, "set_idot: null plan");
+  if (enable != 0 && enable != 1) return fail(COLI_EINVAL, "set_idot: enable must be 0 or 1, got %d", enable);
+  plan->idot = enable;
   return COLI_OK;
 }
 

@@ -29,6 +29,13 @@
 // fp32.  The fixed point keeps every input to within 2^-16 of its block's
 // largest magnitude.
 //
+// Integer-dot inputs (IDOT, both weight types): the activations enter as int8
+// codes q per block of 32 with the block scale 2^(e-6) (warp_quantize_block32_i8);
+// int4 weights take four dp4a per 8-code word pair as above but on one byte
+// plane, int8 weights four dp4a per 16 codes (u8 codes times s8 activations);
+// sum((c - z) q) stays an exact integer and one conversion per block half
+// brings it to fp32.
+//
 // int8 (exact fp32): a code c placed at mantissa bit 4p (int4)
 // or 8p (int8) of the float 2^23 gives 2^23 + c*16^p; subtracting 2^23 leaves
 // c*16^p exactly, and the activation was pre-multiplied by 16^-p (an exact
@@ -200,6 +207,29 @@ __device__ __forceinline__ int dot_row_int4_dp4a(uint4 w, const uint32_t (&xh)[8
   return hi * 256 + (int)lo;
 }
 
+// The same with int8 activation codes (one byte plane): returns sum(c * q) exactly.
+__device__ __forceinline__ int dot_row_int4_i8(uint4 w, const uint32_t (&xq)[8]) {
+  int acc = 0;
+  const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t ev = q[j] & 0x0F0F0F0Fu, od = (q[j] >> 4) & 0x0F0F0F0Fu;
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(ev), "r"(xq[2 * j]));
+    asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(od), "r"(xq[2 * j + 1]));
+  }
+  return acc;
+}
+
+// 16 int8 weight codes (u8, natural order) against 16 int8 activation codes: sum(c * q) exactly.
+__device__ __forceinline__ int dot_row_int8_i8(uint4 w, const uint32_t (&xq)[4]) {
+  int acc = 0;
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(w.x), "r"(xq[0]));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(w.y), "r"(xq[1]));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(w.z), "r"(xq[2]));
+  asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(w.w), "r"(xq[3]));
+  return acc;
+}
+
 __device__ __forceinline__ float pair_sum(uint64_t p) {
   return __uint_as_float((uint32_t)p) + __uint_as_float((uint32_t)(p >> 32));
 }
@@ -308,12 +338,12 @@ __device__ __forceinline__ void store_scales_int4(float2* tab, const ScaleRaw& o
 
 // ------------------------------------------------------------------ one pass (NT tokens, all stages)
 
-template <int QT, bool DOWN, int NT>
+template <int QT, bool DOWN, int NT, bool ID>
 __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_units, int stride, const Cursor& cons,
                                          Cursor& prod, uint8_t* wbuf, uint64_t* bars, float2* tab, int& stage,
                                          uint32_t& phase, uint64_t policy) {
   constexpr bool I4 = QT == COLI_Q_INT4_G128;
-  constexpr bool DP = I4;               // integer dot products (fixed-point activations)
+  constexpr bool DP = I4 || ID;         // integer dot products (fixed-point or int8 activations)
   constexpr int CODES = I4 ? 32 : 16;   // codes per lane per row per stage
   constexpr int XQ = CODES / 4;         // 16-byte activation loads per token
   const int lane = threadIdx.x & 31;
@@ -352,11 +382,16 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
   };
   auto load_x = [&](int t, int code0, ulonglong2 (&xq)[8], float& xsum) {
     const int c = code0 < 0 ? 0 : code0;
-    if constexpr (DP) {   // 64 bytes of hi/lo words (as 4 x 16 bytes) and the block's (sx, sum q)
+    if constexpr (DP) {   // 64 bytes of hi/lo words (as 4 x 16 bytes) and the block's (sx, sum q);
+                          // int8 codes: the 32 bytes of the block (int4) or the lane's 16 (int8)
       const int b = c / kXqBlock;
       const ulonglong2* src = reinterpret_cast<const ulonglong2*>(qrow[t] + (size_t)b * 16);
+      if constexpr (ID && !I4) {
+        xq[0] = __ldg(src + (c % kXqBlock) / 16);
+      } else {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) xq[i] = __ldg(src + i);
+        for (int i = 0; i < (ID ? 2 : 4); ++i) xq[i] = __ldg(src + i);
+      }
       const int2 qs = __ldg(qsrow[t] + b);
       xq[4].x = (unsigned long long)(uint32_t)qs.x | ((unsigned long long)(uint32_t)qs.y << 32);
       return;
@@ -389,7 +424,8 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       int mat, row;
       unit_row<DOWN>(u, lane, mat, row);
       const float s = __ldg(static_cast<const float*>(ex.m[mat].s) + row);
-      tab[lane] = make_float2(s, s * (float)__ldg(ex.m[mat].z + row));
+      const int z = __ldg(ex.m[mat].z + row);
+      tab[lane] = make_float2(s, ID ? __int_as_float(z) : s * (float)z);
     }
     __syncwarp();
   }
@@ -438,7 +474,21 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         if (t > 0) load_x(t, code0, xq, xsum);
-        if (DP) {
+        if constexpr (ID && !I4) {
+          const uint32_t xw[4] = {(uint32_t)xq[0].x, (uint32_t)(xq[0].x >> 32), (uint32_t)xq[0].y,
+                                  (uint32_t)(xq[0].y >> 32)};
+          const float sx = __uint_as_float((uint32_t)xq[4].x);
+          int qs16 = 0;                              // sum of the lane's 16 codes
+#pragma unroll
+          for (int j = 0; j < 4; ++j) asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(qs16) : "r"(0x01010101u), "r"(xw[j]));
+#pragma unroll
+          for (int r = 0; r < kRows; ++r) {
+            const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
+            const float2 sz = tab[r];
+            const int comb = dot_row_int8_i8(w, xw) - __float_as_int(sz.y) * qs16;
+            acc[t][r] = fmaf(sz.x * sx, (float)comb, acc[t][r]);
+          }
+        } else if (DP) {
           uint32_t xh[8], xl[8];
           float sx;
           int qsum;
@@ -455,7 +505,8 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
           for (int r = 0; r < kRows; ++r) {
             const uint4 w = lds128(smem_u32(sbase + stage_off<DOWN>(r, lane >> 4, boxw)));
             const float2 sz = tab[r * kGroupsPerStage + g];
-            const int comb = dot_row_int4_dp4a(w, xh, xl) - __float_as_int(sz.y) * qsum;
+            const int comb = (ID ? dot_row_int4_i8(w, xh) : dot_row_int4_dp4a(w, xh, xl)) -
+                             __float_as_int(sz.y) * qsum;
             acc[t][r] = fmaf(sz.x * sx, (float)comb, acc[t][r]);
           }
         } else {
@@ -492,22 +543,23 @@ __device__ __forceinline__ bool run_pass(const FwdArgs& a, int n_routed, int n_u
       const float up = __shfl_down_sync(0xffffffffu, v, 16);
       const float hv = v / (1.0f + expf(-v)) * up;          // silu(gate) * up
       float hs = hv;                                           // sum of the 8 rows (lanes 0, 2, .., 14)
-      if constexpr (!I4) {
+      if constexpr (!I4 && !ID) {
         hs += __shfl_xor_sync(0xffffffffu, hs, 2);
         hs += __shfl_xor_sync(0xffffffffu, hs, 4);
         hs += __shfl_xor_sync(0xffffffffu, hs, 8);
       }
       const int row = u.rb * 8 + (lane >> 1);
-      // int4: plain h (the down kernel converts it to fixed point); int8: pre-scaled h and its sums
+      // int4 and integer-dot inputs: plain h (quantize_h converts it for the down kernel);
+      // int8: pre-scaled h and its sums
       if (lane < 16 && (lane & 1) == 0 && t < ntok)
-        a.h[(size_t)(p0 + t) * a.Fmax + row] = I4 ? hv : hv * act_prescale(QT, row);
-      if (!I4 && lane == 0 && t < ntok) a.hsum[(size_t)(p0 + t) * (a.Fmax / 8) + u.rb] = hs;
+        a.h[(size_t)(p0 + t) * a.Fmax + row] = (I4 || ID) ? hv : hv * act_prescale(QT, row);
+      if (!I4 && !ID && lane == 0 && t < ntok) a.hsum[(size_t)(p0 + t) * (a.Fmax / 8) + u.rb] = hs;
     }
   }
   return true;
 }
 
-template <int QT, bool DOWN, int NTMAX>
+template <int QT, bool DOWN, int NTMAX, bool ID>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ uint64_t bars_all[kDecodeWarps][kDecodeStages];
@@ -551,10 +603,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   while (cons.valid && ok) {
     const int ntok = min(kMaxNT, cons.u.cnt - cons.pass * kMaxNT);
     if (NTMAX == 1 || ntok <= 1)
-      ok = run_pass<QT, DOWN, 1>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab, stage, phase, policy);
+      ok = run_pass<QT, DOWN, 1, ID>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab, stage, phase,
+                                     policy);
     else
-      ok = run_pass<QT, DOWN, (NTMAX >= 2 ? 2 : 1)>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab, stage,
-                                                   phase, policy);
+      ok = run_pass<QT, DOWN, (NTMAX >= 2 ? 2 : 1), ID>(a, n_routed, n_units, stride, cons, prod, wbuf, bars, tab,
+                                                       stage, phase, policy);
     cons.kb = cons.n_kb - 1;
     cursor_next<QT, DOWN>(a, n_routed, n_units, stride, cons);
   }
@@ -568,24 +621,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1) decode_ffn_kernel(FwdArg
   }
 }
 
-template <int QT, bool DOWN, int NTMAX>
+template <int QT, bool DOWN, int NTMAX, bool ID>
 static cudaError_t launch_decode_t(const FwdArgs& a, cudaStream_t st, int num_sms) {
   const size_t smem = (size_t)kDecodeWarps * kDecodeStages * kStageBytes + 1024;
-  auto kern = decode_ffn_kernel<QT, DOWN, NTMAX>;
+  auto kern = decode_ffn_kernel<QT, DOWN, NTMAX, ID>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kern, dim3(num_sms), dim3(kDecodeWarps * 32), smem, st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <bool DOWN>
-static cudaError_t launch_decode(const FwdArgs& a, int max_tok, cudaStream_t st, int num_sms) {
+template <bool DOWN, bool ID>
+static cudaError_t launch_decode_id(const FwdArgs& a, int max_tok, cudaStream_t st, int num_sms) {
   const bool i4 = a.qtype == COLI_Q_INT4_G128;
   if (max_tok <= 1)
-    return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 1>(a, st, num_sms)
-              : launch_decode_t<COLI_Q_INT8_PC, DOWN, 1>(a, st, num_sms);
-  return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 2>(a, st, num_sms)
-            : launch_decode_t<COLI_Q_INT8_PC, DOWN, 2>(a, st, num_sms);
+    return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 1, ID>(a, st, num_sms)
+              : launch_decode_t<COLI_Q_INT8_PC, DOWN, 1, ID>(a, st, num_sms);
+  return i4 ? launch_decode_t<COLI_Q_INT4_G128, DOWN, 2, ID>(a, st, num_sms)
+            : launch_decode_t<COLI_Q_INT8_PC, DOWN, 2, ID>(a, st, num_sms);
+}
+
+template <bool DOWN>
+static cudaError_t launch_decode(const FwdArgs& a, int max_tok, cudaStream_t st, int num_sms) {
+  return a.idot ? launch_decode_id<DOWN, true>(a, max_tok, st, num_sms)
+                : launch_decode_id<DOWN, false>(a, max_tok, st, num_sms);
 }
 
 cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok, cudaStream_t st, int num_sms) {

@@ -121,6 +121,7 @@ struct FwdArgs {
   float* y;
   unsigned long long wait_ns; // limit of every pipeline wait (kWaitLimitNs unless a test shortens it)
   int inject;                 // COLI_INJECT_* bits of a failure-path test, 0 in normal use
+  int idot;                   // 1: integer-dot inputs (int8 codes per block of 32, power-of-two scale)
 };
 
 // ---------------------------------------------------------------- launchers (one .cu file each)
@@ -130,6 +131,19 @@ cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st);
+// The down kernels' input as floats (colibri_moe_debug_hidden).  mode: 0 decode
+// 16-bit fixed point (int4), 1 decode pre-scaled fp32 (int8), 2 decode int8
+// codes in unpack order (int4, integer-dot), 3 the same in natural order
+// (int8, integer-dot), 4 prefill fp16 (column-permuted when perm).
+struct HiddenView {
+  int mode, perm, qtype, rows, P, F, Fs, Fmax;
+  const float* h;
+  const uint8_t* hq;
+  const int2* hqs;
+  const __half* hh;
+  float* out;
+};
+cudaError_t launch_debug_hidden(const HiddenView& v, cudaStream_t st);
 cudaError_t launch_decode_gateup(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_decode_down(const FwdArgs& a, int max_tok_per_expert, cudaStream_t st, int num_sms);
 cudaError_t launch_combine(const FwdArgs& a, cudaStream_t st);
@@ -301,6 +315,50 @@ __device__ __forceinline__ void warp_quantize_block32(float v, uint8_t* dst, int
   dst[wd * 4 + (j >> 1)] = (uint8_t)((q >> 8) & 255);          // hi (two's complement byte)
   dst[32 + wd * 4 + (j >> 1)] = (uint8_t)(q & 255);             // lo
   if (lane == 0) *qs = make_int2(__float_as_int(sx), sum);
+}
+
+// Integer-dot (IDOT) inputs: one warp quantises one block of 32 values (lane i
+// holds value i) to int8 codes q = rint(v / 2^(e-6)), clamped to [-127, 127],
+// with e = floor(log2(max |v|)) read from the exponent bits of the block's
+// largest magnitude (at least -100, so that 2^(e-6) and 2^(6-e) are normal
+// floats).  v * 2^(6-e) is exact, so the codes do not depend on the
+// arithmetic's precision.  NATURAL: code i at byte i (int8 weights); else in
+// the nibble-unpack order of the int4 kernels (the hi-byte positions of
+// warp_quantize_block32).  qs = (bits of 2^(e-6), sum of the codes).
+template <bool NATURAL>
+__device__ __forceinline__ void warp_quantize_block32_i8(float v, uint8_t* dst, int2* qs) {
+  const int lane = threadIdx.x & 31;
+  float m = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+  e = e < -100 ? -100 : e;
+  const float sx = __uint_as_float((uint32_t)(e - 6 + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(6 - e + 127) << 23);
+  int q = __float2int_rn(v * inv);
+  q = q > 127 ? 127 : (q < -127 ? -127 : q);
+  int sum = q;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (NATURAL) {
+    dst[lane] = (uint8_t)(q & 255);
+  } else {
+    const int j = lane & 7, wd = (lane >> 3) * 2 + (j & 1);
+    dst[wd * 4 + (j >> 1)] = (uint8_t)(q & 255);
+  }
+  if (lane == 0) *qs = make_int2(__float_as_int(sx), sum);
+}
+
+// The IDOT value q * 2^(e-6) of v, given the block's largest magnitude m
+// (prefill: the tensor-core operands carry these values in fp16).
+__device__ __forceinline__ float idot_value(float v, float m) {
+  int e = (int)((__float_as_uint(m) >> 23) & 255u) - 127;
+  e = e < -100 ? -100 : e;
+  const float sx = __uint_as_float((uint32_t)(e - 6 + 127) << 23);
+  const float inv = __uint_as_float((uint32_t)(6 - e + 127) << 23);
+  int q = __float2int_rn(v * inv);
+  q = q > 127 ? 127 : (q < -127 ? -127 : q);
+  return (float)q * sx;
 }
 
 // Programmatic dependent launch: a kernel launched with launch_pdl may start

@@ -92,10 +92,11 @@ cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ int4 decode: h -> fixed point
+// ------------------------------------------------------------------ decode: h -> fixed point / int8 codes
 // The SwiGLU outputs of every grouped pair row (valid columns: F, or F_shared
-// for the shared expert's rows) in the fixed-point layout the int4 down kernel
-// reads, one warp per block of 32 hidden units.
+// for the shared expert's rows) in the layout the down kernel reads, one warp
+// per block of 32 hidden units: the int4 kernels' 16-bit fixed point, or with
+// integer-dot inputs the int8 codes (unpack order for int4, natural for int8).
 __global__ void __launch_bounds__(256) quantize_h_kernel(FwdArgs a) {
   griddep_launch_dependents();
   griddep_wait();                  // h of the gate/up kernel
@@ -107,8 +108,11 @@ __global__ void __launch_bounds__(256) quantize_h_kernel(FwdArgs a) {
     const int r = (int)(b / bpr), c = (int)(b % bpr) * kXqBlock;
     if (c >= (r >= P ? a.Fs : a.F)) continue;          // warp-uniform
     const float v = a.h[(size_t)r * a.Fmax + c + lane];
-    warp_quantize_block32(v, reinterpret_cast<uint8_t*>(a.hq + (size_t)r * (a.Fmax / 2)) + (size_t)(c / kXqBlock) * 64,
-                          a.hqs + (size_t)r * bpr + c / kXqBlock);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(a.hq + (size_t)r * (a.Fmax / 2)) + (size_t)(c / kXqBlock) * 64;
+    int2* qs = a.hqs + (size_t)r * bpr + c / kXqBlock;
+    if (!a.idot) warp_quantize_block32(v, dst, qs);
+    else if (a.qtype == COLI_Q_INT4_G128) warp_quantize_block32_i8<false>(v, dst, qs);
+    else warp_quantize_block32_i8<true>(v, dst, qs);
   }
 }
 
@@ -120,6 +124,43 @@ cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st) {
   if (blocks < 1) blocks = 1;
   const cudaError_t e = launch_pdl(quantize_h_kernel, dim3(blocks), dim3(256), 0, st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ debugging aid: the down kernels' input
+__global__ void __launch_bounds__(256) debug_hidden_kernel(HiddenView v) {
+  const long long n = (long long)v.rows * v.Fmax;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / v.Fmax), c = (int)(i % v.Fmax);
+    float val = 0.f;
+    if (c < (r >= v.P ? v.Fs : v.F)) {
+      if (v.mode == 1) {
+        val = v.h[i] / act_prescale(v.qtype, c);
+      } else if (v.mode == 4) {
+        const int col = v.perm ? ((c & ~7) | ((c & 3) << 1) | ((c >> 2) & 1)) : c;
+        val = __half2float(v.hh[(size_t)r * v.Fmax + col]);
+      } else {
+        const uint8_t* blk = v.hq + (size_t)r * v.Fmax * 2 + (size_t)(c / kXqBlock) * 64;
+        const int2 qs = v.hqs[(size_t)r * (v.Fmax / kXqBlock) + c / kXqBlock];
+        const int l = c % kXqBlock, j = l & 7, wd = (l >> 3) * 2 + (j & 1);
+        const int pos = wd * 4 + (j >> 1);
+        int q;
+        if (v.mode == 0) q = (int)(int8_t)blk[pos] * 256 + (int)blk[32 + pos];
+        else if (v.mode == 2) q = (int)(int8_t)blk[pos];
+        else q = (int)(int8_t)blk[l];
+        val = __int_as_float(qs.x) * (float)q;
+      }
+    }
+    v.out[i] = val;
+  }
+}
+
+cudaError_t launch_debug_hidden(const HiddenView& v, cudaStream_t st) {
+  const long long n = (long long)v.rows * v.Fmax;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  debug_hidden_kernel<<<blocks, 256, 0, st>>>(v);
+  return cudaGetLastError();
 }
 
 }  // namespace coli

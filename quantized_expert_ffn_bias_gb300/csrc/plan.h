@@ -55,6 +55,8 @@ struct coli_moe_plan {
   int last_launches = 0;
   // failure-path testing (colibri_moe_debug_inject)
   int inject = 0;
+  // integer-dot expert inputs (colibri_moe_set_idot)
+  int idot = 0;
   unsigned long long wait_ns = coli::kWaitLimitNs;
 };
 

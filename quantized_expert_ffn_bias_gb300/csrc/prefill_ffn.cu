@@ -81,6 +81,19 @@ __global__ void gather_x_f16_kernel(FwdArgs a, __half* xh, int rows) {
       const float4 f0 = p[0], f1 = p[1];
       v[0] = f0.x; v[1] = f0.y; v[2] = f0.z; v[3] = f0.w; v[4] = f1.x; v[5] = f1.y; v[6] = f1.z; v[7] = f1.w;
     }
+    if (a.idot) {
+      // integer-dot inputs: a block of 32 inputs is held by 4 consecutive lanes (d / 8 is a
+      // multiple of 4 and so is every lane's index, so a group is inside or outside the loop
+      // as a whole); the values q * 2^(e-6) are exact in fp16 for 2^-18 <= max |v| < 2^16
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      const unsigned grp = 0xFu << (threadIdx.x & 28);
+      m = fmaxf(m, __shfl_xor_sync(grp, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(grp, m, 2));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = idot_value(v[j], m);
+    }
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -496,7 +509,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               const float gv = __uint_as_float(r0[i]) * s0, uv = __uint_as_float(r1[i]) * s1;
               // SiLU with the fast exponential and division (relative error ~1e-6, far below the
               // fp16 rounding of h); the epilogue shares issue slots with the dequantising warps
-              const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+              if (a.idot) {      // integer-dot inputs: the warp's 32 rows are one block of 32 hidden units
+                float m = fabsf(hv);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                hv = idot_value(hv, m);
+              }
               p.hout[(size_t)(row0 + tcol) * a.Fmax + hcol] = __float2half_rn(hv);
             }
           }

@@ -372,15 +372,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
   };
   load_batch(lane * 4);
   // (1) dequant-GEMV inputs, grid-stride: int4 -> 16-bit fixed point per block
-  //     of kXqBlock inputs (one warp per block); int8 -> pre-scaled fp32 + block sums
-  if (a.qtype == COLI_Q_INT4_G128) {
+  //     of kXqBlock inputs (one warp per block); int8 -> pre-scaled fp32 + block sums;
+  //     integer-dot inputs (both weight types) -> int8 codes per block
+  if (a.qtype == COLI_Q_INT4_G128 || a.idot) {
     const int nblk = a.T * a.d / kXqBlock;
     const int nw = gridDim.x * (kRouteThreads / 32);
     for (int b = (blockIdx.x * kRouteThreads + tid) >> 5; b < nblk; b += nw) {
       const int i = b * kXqBlock + lane;
       const float v = XT == COLI_X_BF16 ? __uint_as_float((uint32_t)static_cast<const uint16_t*>(a.x)[i] << 16)
                                         : static_cast<const float*>(a.x)[i];
-      warp_quantize_block32(v, reinterpret_cast<uint8_t*>(a.xq) + (size_t)b * 64, a.xqs + b);
+      uint8_t* dst = reinterpret_cast<uint8_t*>(a.xq) + (size_t)b * 64;
+      if (!a.idot) warp_quantize_block32(v, dst, a.xqs + b);
+      else if (a.qtype == COLI_Q_INT4_G128) warp_quantize_block32_i8<false>(v, dst, a.xqs + b);
+      else warp_quantize_block32_i8<true>(v, dst, a.xqs + b);
     }
   } else {
     const int n = a.T * a.d;

@@ -604,6 +604,9 @@ def pin_idot_expert_brute_force(L=None):
                     a[:] = 1.5 * st
                 amb.append(a)
             hq, amb = np.concatenate(hq), np.concatenate(amb)
+            oh, ohq, oamb = O.idot_hidden(layer.experts, e, xt, tau, L=L)
+            assert np.allclose(oh, h, rtol=1e-12, atol=1e-15), (qt, e)
+            assert np.array_equal(ohq, hq) and np.array_equal(oamb, amb), (qt, e)
             assert np.allclose(y, Wd[e] @ hq, rtol=1e-11, atol=1e-13), (qt, e)
             assert np.allclose(yb, np.abs(Wd[e]) @ amb, rtol=1e-11, atol=1e-15), (qt, e)
 

@@ -51,6 +51,8 @@ MUTANTS = {
     "idot_x_unquantised": ("for (int i = 0; i < d; ++i) a += w[i] * xq[i];",
                            "for (int i = 0; i < d; ++i) a += w[i] * x[i];"),
     "idot_h_unquantised": ("acc += w[n] * hq[n];", "acc += w[n] * h[n];"),
+    "idot_hidden_skips_block": ("for (int b = 0; b < F; b += 32) orc_mx8_block(32, h + b, tau, hq + b, amb + b);",
+                                "for (int b = 0; b < F - 32; b += 32) orc_mx8_block(32, h + b, tau, hq + b, amb + b);"),
     "idot_bound_signed": ("bnd += fabs(w[n]) * amb[n];", "bnd += w[n] * amb[n];"),
     "idot_block_tie_one_side": ("block_amb = (r - 1.0 < tau / 64.0) || (2.0 - r < tau / 64.0);",
                                 "block_amb = (r - 1.0 < tau / 64.0);"),
