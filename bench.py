@@ -14,6 +14,7 @@ routing statistics (near-tie tokens, unique experts per step).
 
   decode + cache    decode T=1 with every expert in pinned host memory behind 32 device slots (weighted LRU)
   decode + pilot    two such layers, layer 1's experts predicted from layer 0's input and read ahead
+  IDOT              decode T=1 and prefill T=2048 with integer-dot expert inputs (int8 per block of 32)
   indexer T=1 / T=4 sparse-attention key selection: 64 heads of 128, 65,536 cached keys, top-2048
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|mtp_verify|prefill|stacked|indexer]
@@ -274,7 +275,11 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
     K, W = args.steps, args.warmup
     pk = peaks()
     frags = {}
-    for T in Ts:
+    runs = [(T, False) for T in Ts]
+    if name in ("decode", "prefill") and not args.experts and not args.tokens and not args.no_idot:
+        runs.append((Ts[0], True))      # integer-dot expert inputs on the same layer
+    for T, idot in runs:
+        dl.plan.set_idot(idot)
         xs = [to_dev(w.x(T, 1000 + i), dev) for i in range(K + W)]
         out = torch.empty((T, layer.d), dtype=torch.float32, device=dev)
 
@@ -331,7 +336,7 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
                     else None,
                     "peak_source": pk["source"], "algorithmic_bytes_per_launch": gub / max(gu_n, 1),
                     "down_kernel_achieved_gbs": achieved_d}
-        frags[T] = {
+        frags[(T, "idot") if idot else T] = {
             "value": replica_tokens_per_s(world, K, T, ms_tot),
             "unit": "tokens/s",
             "ms_per_step": ms_tot / K,
@@ -346,9 +351,12 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
             "clocks": clocks,
             "routing": {"tokens": K * T, "near_tie_tokens": near, "unique_experts_per_step": uniq / K,
                         "near_tie_rule": "k-th minus (k+1)-th selection score < 1e-5, flagged by the GPU router"},
-            "config": workload_config(w, T, world),
+            "config": dict(workload_config(w, T, world),
+                           **({"activations": "integer-dot: int8 codes per block of 32, power-of-two scale"}
+                              if idot else {})),
         }
         del xs
+    dl.plan.set_idot(False)
     cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
     if name == "decode" and not args.experts and not args.tokens and not args.no_cache:
         frags["cache"] = bench_cache(dl, layer, w, args, dev, world)
@@ -898,6 +906,7 @@ def main():
                          "stacked layers as variants; otherwise that workload alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cache", action="store_true", help="skip the expert-cache variant of the decode workload")
+    ap.add_argument("--no-idot", action="store_true", help="skip the integer-dot variants of decode and prefill")
     ap.add_argument("--experts", type=int, default=0, help="override E (reduced case for profiler captures)")
     ap.add_argument("--tokens", type=int, default=0, help="override T (reduced case for profiler captures)")
     args = ap.parse_args()
@@ -936,6 +945,9 @@ def main():
                     continue
                 if T == "pilot":
                     results.append(("decode T=1, 2 layers, expert caches + next-layer prediction", name, 1, fr))
+                    continue
+                if isinstance(T, tuple):
+                    results.append((f"{name} T={T[0]} integer-dot (IDOT)", name, T[0], fr))
                     continue
                 fr["cpu_baseline"] = cpu if i == 0 else None
                 results.append((f"{name} T={T}", name, T, fr))

@@ -317,7 +317,8 @@ struct PfLayout {
   static_assert(kAStages * kAStageCols + kPfACol <= 512, "TMEM budget");
 };
 
-template <int QT, bool GU>
+// ID (gate/up only): integer-dot inputs, h leaves the epilogue as its IDOT values
+template <int QT, bool GU, bool ID>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefill_ffn_kernel(FwdArgs a, PfArgs p, const __grid_constant__ CUtensorMap bmap) {
   using L = PfLayout<QT, GU>;
@@ -510,10 +511,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
               // SiLU with the fast exponential and division (relative error ~1e-6, far below the
               // fp16 rounding of h); the epilogue shares issue slots with the dequantising warps
               float hv = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-              if (a.idot) {      // integer-dot inputs: the warp's 32 rows are one block of 32 hidden units
-                float m = fabsf(hv);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+              if constexpr (ID) {   // the warp's 32 rows are one block of 32 hidden units; the block's
+                                    // largest magnitude (non-negative floats order as their bits)
+                const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv))));
                 hv = idot_value(hv, m);
               }
               p.hout[(size_t)(row0 + tcol) * a.Fmax + hcol] = __float2half_rn(hv);
@@ -670,13 +670,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-template <int QT, bool GU>
+template <int QT, bool GU, bool ID = false>
 static cudaError_t launch_pf(const FwdArgs& a, const PfArgs& p, const CUtensorMap& bmap, cudaStream_t st,
                              int num_sms) {
   using L = PfLayout<QT, GU>;
   const size_t smem = (size_t)L::kSmemBytes + 1024;
   static_assert(L::kSmemBytes + 1024 <= 227 * 1024, "shared memory");
-  auto kern = prefill_ffn_kernel<QT, GU>;
+  auto kern = prefill_ffn_kernel<QT, GU, ID>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<num_sms, kPfThreads, smem, st>>>(a, p, bmap);
@@ -703,6 +703,9 @@ cudaError_t launch_prefill_gateup(const FwdArgs& a, const void* chunks, const vo
                                   const CUtensorMap* wmaps, const CUtensorMap& xmap, __half* hout, cudaStream_t st,
                                   int num_sms) {
   PfArgs p{static_cast<const PfChunk*>(chunks), static_cast<const PfTile*>(tiles), n_tiles, wmaps, hout, nullptr};
+  if (a.idot)
+    return a.qtype == COLI_Q_INT4_G128 ? launch_pf<COLI_Q_INT4_G128, true, true>(a, p, xmap, st, num_sms)
+                                       : launch_pf<COLI_Q_INT8_PC, true, true>(a, p, xmap, st, num_sms);
   return a.qtype == COLI_Q_INT4_G128 ? launch_pf<COLI_Q_INT4_G128, true>(a, p, xmap, st, num_sms)
                                      : launch_pf<COLI_Q_INT8_PC, true>(a, p, xmap, st, num_sms);
 }
