@@ -822,7 +822,7 @@ def bench_indexer(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
             "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s",
                     "h2d_bytes_per_step": qh[0].numel() * qh[0].element_size() + wh[0].numel() * 4,
                     "d2h_bytes_per_step": T * w.topk * 4},
-            "gpu_launches": K * (n_groups + 1),
+            "gpu_launches": K * (n_groups + 2),     # score kernel per group of 4 queries, mark, finish
             "clocks": clk.summary(),
             "config": {"workload": f"indexer: sparse-attention key selection (scores + top-{w.topk}) for T={T} "
                                    f"query tokens over {L} cached keys", "heads": w.H, "head_dim": w.d,

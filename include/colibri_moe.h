@@ -223,6 +223,7 @@ COLI_API coli_status colibri_moe_debug_routing(const coli_moe_plan_t* plan, cons
  */
 #define COLI_DEV_BAD_EXPERT_ID 1   /* a router index outside [0, E) reached the grouping step */
 #define COLI_DEV_WAIT_TIMEOUT 2    /* a pipeline wait gave up after its time limit (~1 s) */
+#define COLI_DEV_SELECT_ROUNDS 4   /* the key selection's rounds did not narrow to one value (not expected) */
 COLI_API coli_status colibri_moe_check_status(const coli_moe_plan_t* plan, const void* workspace, int32_t* device_status,
                                      void* stream);
 
@@ -402,13 +403,13 @@ COLI_API coli_status colibri_moe_cache_simulate(int E, int n_slots, double weigh
  *            -1 padded when a query sees fewer than topk keys.
  *   workspace device, >= colibri_indexer_workspace_size(T, L) bytes, 256-byte
  *            aligned.  Layout: int32 status word at offset 0; the fp32 scores
- *            [T][L] at offset 256 (-infinity where a key is not visible);
- *            then a 65536-bin histogram of each query's scores (selection).
+ *            [T][L] at offset 256 (-infinity where a key is not visible).
  * This build serves H = 64 heads of d = 128 and L <= 131072 keys
  * (COLI_EUNSUPPORTED otherwise).
  * Asynchronous on stream; errors: COLI_EINVAL, COLI_EALIGN, COLI_EWORKSPACE,
  * COLI_EUNSUPPORTED, COLI_ECUDA.  colibri_indexer_check_status reads the
- * status word (COLI_DEV_WAIT_TIMEOUT if a pipeline wait gave up).
+ * status word (COLI_DEV_WAIT_TIMEOUT if a pipeline wait gave up,
+ * COLI_DEV_SELECT_ROUNDS if the selection did not converge).
  */
 COLI_API coli_status colibri_indexer_workspace_size(int T_max, int L_max, size_t* bytes);
 COLI_API coli_status colibri_indexer_topk(int T, int L, int pos0, int H, int d, int topk, const void* q, const float* w,

@@ -504,8 +504,7 @@ int colibri_moe_last_launch_count(const coli_moe_plan_t* plan) { return plan ? p
 // status | scores [T][L] | counts [T] | histogram [T][65536] | coarse histogram [T][2048] |
 // bitmask [T][ceil(L/32)] | candidates [T][2048] x 2   (counts and histograms adjoin: one clear covers them)
 static size_t indexer_ws_bytes(int T, int L) {
-  return 256 + align_up((size_t)T * (size_t)L * 4, 256) + align_up((size_t)T * 4, 256) + (size_t)T * 65536 * 4 +
-         (size_t)T * 2048 * 4 + align_up((size_t)T * ((L + 31) / 32) * 4, 256) + (size_t)T * 2048 * 8;
+  return 256 + align_up((size_t)T * (size_t)L * 4, 256);
 }
 
 coli_status colibri_indexer_workspace_size(int T_max, int L_max, size_t* bytes) {
@@ -539,23 +538,8 @@ static coli_status indexer_call(int steps, int T, int L, int pos0, int H, int d,
   if (ce != cudaSuccess) return cuda_fail(ce, "indexer_topk: device query");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const size_t off_counts = 256 + align_up((size_t)T * (size_t)L * 4, 256);
-  size_t off = off_counts;
-  int* cand_n = reinterpret_cast<int*>(ws + off);
-  off += align_up((size_t)T * 4, 256);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(ws + off);
-  off += (size_t)T * 65536 * 4;
-  uint32_t* chist = reinterpret_cast<uint32_t*>(ws + off);
-  off += (size_t)T * 2048 * 4;
-  const size_t off_cleared_end = off;
-  uint32_t* sel_bits = reinterpret_cast<uint32_t*>(ws + off);
-  off += align_up((size_t)T * ((L + 31) / 32) * 4, 256);
-  float* cand_val = reinterpret_cast<float*>(ws + off);
-  off += (size_t)T * 2048 * 4;
-  int* cand_idx = reinterpret_cast<int*>(ws + off);
   if (steps & 1) {
     ce = cudaMemsetAsync(ws, 0, 64, st);
-    if (ce == cudaSuccess) ce = cudaMemsetAsync(ws + off_counts, 0, off_cleared_end - off_counts, st);
     if (ce != cudaSuccess) return cuda_fail(ce, "indexer_topk: clear status");
   }
   IndexerCall c;
@@ -567,12 +551,6 @@ static coli_status indexer_call(int steps, int T, int L, int pos0, int H, int d,
   c.w = w;
   c.keys = keys;
   c.scores = reinterpret_cast<float*>(ws + 256);
-  c.hist = hist;
-  c.chist = chist;
-  c.sel_bits = sel_bits;
-  c.cand_val = cand_val;
-  c.cand_idx = cand_idx;
-  c.cand_n = cand_n;
   c.out = topk_idx;
   c.status = reinterpret_cast<int32_t*>(ws);
   c.wait_ns = kWaitLimitNs;

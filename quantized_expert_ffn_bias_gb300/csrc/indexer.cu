@@ -16,12 +16,10 @@
 // order) and the causal mask.  Double-buffered accumulators let the MMAs of one
 // tile overlap the epilogue of the previous one.  All waits are bounded.
 //
-// Top-k: the score kernel also counts every visible score in a 65536-bin
-// histogram of the top 16 bits of its order-preserving integer image.  A
-// marking kernel (16 CTAs per query at 65,536 keys) finds the bin of the
-// topk-th score from it, sets the bits of the keys above that bin in a key
-// bitmask and gathers the keys in it; one CTA per query then ranks those
-// exactly (score, then key index) and writes the bitmask out in key order.
+// Top-k: one thread-block cluster of 8 CTAs per query runs an exact bucket
+// select on the scores' order-preserving integer images held in shared
+// memory, with the cluster's counts summed through distributed shared memory
+// (see the selection kernel).
 #include "moe_internal.cuh"
 
 namespace coli {
@@ -34,15 +32,12 @@ constexpr int kIxStages = 4;
 constexpr int kIxThreads = 6 * 32;
 constexpr int kIxAtomKeys = kIxKeys * 128;            // bytes of one 64-element atom of a key tile
 constexpr int kIxStageBytes = 2 * kIxAtomKeys;        // 32 KB
-constexpr int kIxTopkThreads = 1024;
 
 struct IxArgs {
   int T, L, pos0;
   const float* w;        // [T][64] head weights of this launch's queries
   float* scores;         // [T][ls]
   int ls;
-  uint32_t* hist;        // [T][65536]: visible scores per top 16 bits of their integer image (cleared before)
-  uint32_t* chist;       // [T][2048]: the same per top 11 bits (cleared before)
   int32_t* status;
   unsigned long long wait_ns;
 };
@@ -55,6 +50,8 @@ __device__ __forceinline__ uint32_t ix_key(float v) {
 __device__ __forceinline__ float ix_unkey(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
+
+
 
 __device__ __forceinline__ uint64_t ix_desc_sw128(uint32_t saddr) {
   uint64_t d = 0;
@@ -97,7 +94,6 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   __shared__ uint64_t full[kIxStages], empty[kIxStages], q_full, acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ float ws[kIxQMax * kIxHeads];
-  __shared__ uint32_t ch[kIxQMax][1024];   // this CTA's share of the coarse histogram, two 16-bit counts a word
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* qs = smem + kIxStages * kIxStageBytes;   // queries: two atoms of N rows x 128 bytes
@@ -120,7 +116,6 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < p.T * kIxHeads; i += blockDim.x) ws[i] = p.w[i];
-  for (int i = threadIdx.x; i < p.T * 1024; i += blockDim.x) (&ch[0][0])[i] = 0u;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                  "r"(512));
@@ -213,13 +208,6 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         for (int j = 0; j < kIxHeads; ++j) sum = fmaf(ws[q * kIxHeads + j], fmaxf(__uint_as_float(r[j]), 0.f), sum);
         const bool vis = s < p.L && s <= p.pos0 + q;
         if (s < p.L) p.scores[(size_t)q * p.ls + s] = vis ? sum : -INFINITY;
-        // the selection's histograms: top 16 bits of the score's order-preserving image (global) and
-        // top 11 bits (this CTA's share, added to the global one at the end)
-        if (vis) {
-          const uint32_t key = ix_key(sum);
-          atomicAdd(p.hist + ((size_t)q << 16) + (key >> 16), 1u);
-          atomicAdd(&ch[q][key >> 22], 1u << (16 * ((key >> 21) & 1)));   // < 2^16 keys per CTA and query
-        }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
@@ -232,292 +220,314 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
-  for (int i = threadIdx.x; i < p.T * 1024; i += blockDim.x) {
-    const uint32_t v = (&ch[0][0])[i];
-    if (v & 0xFFFFu) atomicAdd(p.chist + 2 * i, v & 0xFFFFu);
-    if (v >> 16) atomicAdd(p.chist + 2 * i + 1, v >> 16);
-  }
 }
 
-// ------------------------------------------------------------------ top-k (one CTA per query)
+// ------------------------------------------------------------------ top-k: one cluster of CTAs per query
+//
+// kIxSelCtas CTAs (one thread-block cluster) share a query's visible keys in contiguous ranges and keep
+// their keys' integer images in shared memory.  An exact bucket select runs over the cluster: the
+// cluster's smallest and largest image bound the range; each round every CTA counts its keys of the
+// current range in 2048 equal-width bins, the CTAs sum the cluster's counts through distributed shared
+// memory, and the bin holding the topk-th largest key becomes the next range; at most three rounds bring
+// the range to one value (2^32 / 2048^2 < 2048).  Keys above that value are taken, and keys equal to it
+// in ascending key order until topk keys are taken (a tie goes to the lower key).  A cluster prefix of
+// the CTAs' counts places each CTA's keys in the ascending output.  Cluster barriers are hardware
+// barriers; no CTA leaves while another may still read its shared memory.
 
-constexpr int kIxMaxKeys = 1 << 17;      // keys one selection serves (the key bitmask lives in shared memory)
-constexpr int kIxCand = 2048;            // candidates of the boundary bin kept in shared memory
-constexpr int kIxBatch = 16;             // rounds of scores loaded ahead in the selection passes
-
-// Bin (of nb) of the rem-th largest element and the rank `rem` within it, from a histogram in shared
-// memory.  All threads call it; the result is in *s_bin / *s_rem after it returns.
-__device__ __forceinline__ void ix_find_bin(const int* hist, int nb, int rem, int* warp_tot, int* total,
-                                            int* s_bin, int* s_rem) {
-  const int tid = threadIdx.x, nthr = blockDim.x;
-  const int per = nb / nthr > 0 ? nb / nthr : 1;   // bins per thread, from the top down
-  const int first = nb - 1 - tid * per;
-  int c = 0;
-  if (tid * per < nb)
-    for (int j = 0; j < per; ++j) c += hist[first - j];
-  const int above = block_exclusive_scan(c, warp_tot, total);
-  if (tid * per < nb && above < rem && rem <= above + c) {
-    int cum = above;
-    for (int j = 0; j < per; ++j) {
-      const int b = first - j;
-      if (cum + hist[b] >= rem) {
-        *s_bin = b;
-        *s_rem = rem - cum;
-        break;
-      }
-      cum += hist[b];
-    }
-  }
-  __syncthreads();
-}
-
-// Warp-aggregated shared-memory histogram increment: lanes with the same bin add once.
-__device__ __forceinline__ void ix_hist_add(int* hist, int bin, bool active) {
-  const unsigned act = __ballot_sync(0xffffffffu, active);
-  if (!active) return;
-  const unsigned peers = __match_any_sync(act, bin);
-  if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-}
-
-constexpr int kIxChunk = 4096;           // keys per CTA of the marking kernel
-constexpr int kIxMarkThreads = 256;
+constexpr int kIxSelCtas = 8;            // CTAs per query (portable cluster size)
+constexpr int kIxSelThreads = 512;
+constexpr int kIxBins = 2048;
+constexpr int kIxGroups = kIxBins / 32;  // group sums exchanged first (a group: 32 bins)
 
 struct IxSel {
   const float* scores;     // [T][ls]
   int ls, L, pos0, topk;
-  const uint32_t* hist;    // [T][65536]
-  const uint32_t* chist;   // [T][2048]
-  uint32_t* bits;          // [T][ws_words] selected-key bitmask (keys above the boundary bin)
-  int ws_words;
-  float* cand_val;         // [T][kIxCand] boundary-bin keys
-  int* cand_idx;
-  int* cand_n;             // [T] (cleared before the scores are computed)
+  int chunk;               // keys per CTA (a multiple of 32)
   int32_t* out;            // [T][topk]
+  int32_t* status;
 };
 
-__device__ __forceinline__ int ix_visible(const IxSel& p, int q) {
-  const long long v = (long long)p.pos0 + q + 1;   // keys s <= pos0 + q, s < L
-  return v < p.L ? (int)v : p.L;
+__device__ __forceinline__ void ix_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Bin of the topk-th largest score: the query's 2048-bin histogram (top 11 bits of the integer image),
-// scanned from the top by the whole CTA, names the coarse bin; warp 0 then scans the 32 fine bins (top 16
-// bits) inside it.  (bin, rank within it, keys in it) land in shared memory.
-__device__ __forceinline__ void ix_boundary(const uint32_t* gh, const uint32_t* gch, int topk, int* warp_tot,
-                                            int* total, int* s_bin, int* s_rem, int* s_cnt, int* s_run) {
-  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
-  const int per = 2048 / nthr;             // coarse bins per thread (8 or 2)
-  const int top = 2047 - tid * per;
-  int h[8];
-  int c = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {            // h[i]: bin top - i
-    h[i] = i < per ? (int)__ldcg(gch + top - i) : 0;
-    c += h[i];
-  }
-  const int above = block_exclusive_scan(c, warp_tot, total);
-  if (above < topk && topk <= above + c) {
-    int cum = above;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i < per && cum + h[i] >= topk) {
-        s_run[0] = top - i;                // coarse bin
-        s_run[1] = cum;                    // keys in higher coarse bins
-        break;
-      }
-      cum += h[i];
-    }
-  }
-  __syncthreads();
-  if (tid < 32) {
-    const int cb = s_run[0];
-    const int fb = cb * 32 + 31 - lane;    // lane 0: the highest fine bin of the coarse bin
-    const int hf = (int)__ldcg(gh + fb);
-    int inc = hf;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, inc, o);
-      if (lane >= o) inc += n;
-    }
-    const int cum = s_run[1] + inc - hf;
-    if (cum < topk && topk <= cum + hf) {
-      *s_bin = fb;
-      *s_rem = topk - cum;
-      *s_cnt = hf;
-    }
-  }
-  __syncthreads();
+// Generic address of shared variable `p` in CTA `rank` of this cluster.  Loads through it are ordinary
+// loads: the compiler may batch them, and the cluster barrier (a memory clobber) orders them after it.
+template <typename T>
+__device__ __forceinline__ const T* ix_peer(const T* p, uint32_t rank) {
+  uint64_t a;
+  asm("mapa.u64 %0, %1, %2;" : "=l"(a) : "l"(reinterpret_cast<uint64_t>(p)), "r"(rank));
+  return reinterpret_cast<const T*>(a);
 }
 
-// Grid (chunks of kIxChunk keys, queries): keys above the boundary bin set their bit in the query's
-// bitmask (warp ballots), keys in it are appended to the query's candidate list (warp-aggregated).
-__global__ void __launch_bounds__(kIxMarkThreads) indexer_mark_kernel(IxSel p) {
+__global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel p) {
+  // per round and bin: keys, smallest and largest image (ping-pong: a peer may still read the previous
+  // round's), then this CTA's keys' integer images
+  extern __shared__ __align__(16) uint32_t dyn[];
+  uint32_t(*cnt)[kIxBins] = reinterpret_cast<uint32_t(*)[kIxBins]>(dyn);
+  uint32_t(*bmin)[kIxBins] = reinterpret_cast<uint32_t(*)[kIxBins]>(dyn + 2 * kIxBins);
+  uint32_t(*bmax)[kIxBins] = reinterpret_cast<uint32_t(*)[kIxBins]>(dyn + 4 * kIxBins);
+  uint32_t* u_s = dyn + 6 * kIxBins;
+  __shared__ uint32_t ex[4];                            // exchanged: min image, max image, keys above, keys equal
+  __shared__ uint32_t gsum[2][kIxGroups], gtot[kIxGroups];
+  __shared__ uint32_t s_lo, s_hi;
+  __shared__ int s_rem;
   __shared__ int warp_tot[32];
-  __shared__ int total, s_bin, s_rem, s_cnt, s_run[2];
-  const int q = blockIdx.y, lane = threadIdx.x & 31;
-  const int vis = ix_visible(p, q);
-  const int k0 = blockIdx.x * kIxChunk;
-  if (vis <= p.topk || k0 >= vis) return;          // (block-uniform)
-  ix_boundary(p.hist + ((size_t)q << 16), p.chist + ((size_t)q << 11), p.topk, warp_tot, &total, &s_bin, &s_rem,
-              &s_cnt, s_run);
-  const uint32_t bin = (uint32_t)s_bin;
-  const bool keep = s_cnt <= kIxCand;               // otherwise the finishing kernel takes the long way
-  const float* sc = p.scores + (size_t)q * p.ls;
-  uint32_t* bits = p.bits + (size_t)q * p.ws_words;
-  constexpr int kPer = kIxChunk / kIxMarkThreads;
-  float vb[kPer];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int s = k0 + i * kIxMarkThreads + threadIdx.x;
-    vb[i] = s < vis ? sc[s] : 0.f;
-  }
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const int s = k0 + i * kIxMarkThreads + threadIdx.x;
-    const bool valid = s < vis;
-    const uint32_t b = valid ? ix_key(vb[i]) >> 16 : 0u;
-    const unsigned word = __ballot_sync(0xffffffffu, valid && b > bin);
-    if (lane == 0 && s < vis) bits[s >> 5] = word;
-    const unsigned cm = keep ? __ballot_sync(0xffffffffu, valid && b == bin) : 0u;
-    if (cm) {
-      int base = 0;
-      if (lane == __ffs(cm) - 1) base = atomicAdd(p.cand_n + q, __popc(cm));
-      base = __shfl_sync(0xffffffffu, base, __ffs(cm) - 1);
-      if (valid && b == bin) {
-        const int c = base + __popc(cm & ((1u << lane) - 1u));
-        if (c < kIxCand) {   // the bin holds s_cnt <= kIxCand keys in all
-          p.cand_val[(size_t)q * kIxCand + c] = vb[i];
-          p.cand_idx[(size_t)q * kIxCand + c] = s;
-        }
-      }
-    }
-  }
-}
-
-// One CTA per query: the boundary-bin candidates ranked exactly (score descending, key ascending), the
-// first `rem` added to the bitmask, and the bitmask written out in key order.  A boundary bin with more
-// keys than the candidate list holds (many equal or near-equal scores) takes the long way: an exact
-// radix select on the integer image (11 + 11 + 10 bits over three passes) gives the threshold, and one
-// marking pass takes the keys above it and, in key order, the first keys equal to it.
-__global__ void __launch_bounds__(kIxTopkThreads) indexer_finish_kernel(IxSel p) {
-  __shared__ uint32_t bits[kIxMaxKeys / 32];
-  __shared__ int hist[2048];
-  __shared__ float cand_val[kIxCand];
-  __shared__ int cand_idx[kIxCand];
-  __shared__ int warp_tot[32];
-  __shared__ int total, s_bin, s_rem, s_cnt, s_eq, s_run[2];
-  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31;
-  const int q = blockIdx.x;
-  const float* sc = p.scores + (size_t)q * p.ls;
-  int32_t* o = p.out + (size_t)q * p.topk;
-  const int vis = ix_visible(p, q), topk = p.topk;
-  if (vis <= topk) {
-    for (int i = tid; i < topk; i += nthr) o[i] = i < vis ? i : -1;
+  __shared__ int total;
+  const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5, nw = nthr >> 5;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int q = blockIdx.y;
+  const long long v = (long long)p.pos0 + q + 1;          // keys s <= pos0 + q, s < L
+  const int vis = v < p.L ? (int)v : p.L;
+  const int topk = p.topk;
+  int32_t* o = p.out + (size_t)q * topk;
+  if (vis <= topk) {                                      // cluster-uniform: every visible key, then -1
+    for (int i = (int)rank * nthr + tid; i < topk; i += kIxSelCtas * nthr) o[i] = i < vis ? i : -1;
     return;
   }
-  const int nwords = (vis + 31) / 32;
-  const int rounds = (vis + nthr - 1) / nthr;
-  ix_boundary(p.hist + ((size_t)q << 16), p.chist + ((size_t)q << 11), topk, warp_tot, &total, &s_bin, &s_rem,
-              &s_cnt, s_run);
-  int rem = s_rem;
-  if (s_cnt <= kIxCand) {
-    const uint32_t* gbits = p.bits + (size_t)q * p.ws_words;
-    for (int i = tid; i < nwords; i += nthr) bits[i] = __ldcg(gbits + i);
-    const int nc = s_cnt;
-    for (int c = tid; c < nc; c += nthr) {
-      cand_val[c] = __ldcg(p.cand_val + (size_t)q * kIxCand + c);
-      cand_idx[c] = __ldcg(p.cand_idx + (size_t)q * kIxCand + c);
+  const int k0 = (int)rank * p.chunk;
+  const int n = max(0, min(vis, k0 + p.chunk) - k0);
+  const float* sc = p.scores + (size_t)q * p.ls + k0;
+
+  // load the images; the CTA's smallest and largest, then the cluster's
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int i = tid; i < n; i += nthr) {
+    const uint32_t u = ix_key(__ldcg(sc + i));
+    u_s[i] = u;
+    mn = min(mn, u);
+    mx = max(mx, u);
+  }
+  mn = __reduce_min_sync(0xffffffffu, mn);
+  mx = __reduce_max_sync(0xffffffffu, mx);
+  if (lane == 0) {
+    cnt[0][wid] = mn;
+    cnt[1][wid] = mx;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    mn = __reduce_min_sync(0xffffffffu, lane < nw ? cnt[0][lane] : 0xFFFFFFFFu);
+    mx = __reduce_max_sync(0xffffffffu, lane < nw ? cnt[1][lane] : 0u);
+    if (lane == 0) {
+      ex[0] = mn;
+      ex[1] = mx;
+    }
+  }
+  ix_cluster_sync();                                      // (1) every CTA's bounds are visible
+  if (wid == 0) {
+    mn = __reduce_min_sync(0xffffffffu, lane < kIxSelCtas ? *ix_peer(&ex[0], lane) : 0xFFFFFFFFu);
+    mx = __reduce_max_sync(0xffffffffu, lane < kIxSelCtas ? *ix_peer(&ex[1], lane) : 0u);
+    if (lane == 0) {
+      s_lo = mn;
+      s_hi = mx;
+    }
+  }
+  __syncthreads();
+
+  // rounds: the keys with images in [lo, hi] hold the wanted key at rank `rem` from the top; 2048 bins over
+  // the range (round 0 linear in the score value, then linear in the image), counted per CTA, summed over
+  // the cluster; the bin holding rank `rem` becomes the range, bounded by its keys' smallest and largest
+  // images.  The range shrinks by at least 2048 per image round, so it ends at one value.
+  uint32_t lo = s_lo, hi = s_hi;
+  int rem = topk;
+  constexpr int kMaxRounds = 8;                          // 4 suffice (one value round, three image rounds)
+  for (int round = 0; lo < hi && round < kMaxRounds; ++round) {
+    const int pb = round & 1;
+    const float vlo = ix_unkey(lo), vhi = ix_unkey(hi);
+    const float vscale = (float)kIxBins / (vhi - vlo);
+    const bool by_value = round == 0 && vscale > 0.f && vscale < INFINITY;
+    const uint32_t width = (uint32_t)((((uint64_t)hi - lo) >> 11) + 1);
+    for (int b = tid; b < kIxBins; b += nthr) {
+      cnt[pb][b] = 0u;
+      bmin[pb][b] = 0xFFFFFFFFu;
+      bmax[pb][b] = 0u;
     }
     __syncthreads();
-    for (int c = tid; c < nc; c += nthr) {
-      const float v = cand_val[c];
-      const int si = cand_idx[c];
-      int rank = 0;
-      for (int e = 0; e < nc; ++e) rank += cand_val[e] > v || (cand_val[e] == v && cand_idx[e] < si);
-      if (rank < rem) atomicOr(&bits[si >> 5], 1u << (si & 31));
-    }
-    __syncthreads();
-  } else {
-    for (int i = tid; i < nwords; i += nthr) bits[i] = 0u;
-    uint32_t prefix = 0, mask = 0;
-    rem = topk;
-    for (int pass = 0; pass < 3; ++pass) {
-      const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0), w = pass == 2 ? 10 : 11;
-      const uint32_t bm = (1u << w) - 1u;
-      __syncthreads();
-      for (int b = tid; b < 2048; b += nthr) hist[b] = 0;
-      __syncthreads();
-      for (int r = 0; r < rounds; ++r) {
-        const int s = r * nthr + tid;
-        const uint32_t u = s < vis ? ix_key(sc[s]) : 0u;
-        const bool hit = s < vis && (u & mask) == prefix;
-        ix_hist_add(hist, hit ? (int)((u >> sh) & bm) : 0, hit);
+    for (int i = tid; i < n; i += nthr) {
+      const uint32_t u = u_s[i];
+      if (u < lo || u > hi) continue;
+      int b;
+      if (by_value) {
+        b = (int)((ix_unkey(u) - vlo) * vscale);
+        b = b < 0 ? 0 : (b > kIxBins - 1 ? kIxBins - 1 : b);
+      } else {
+        b = (int)((u - lo) / width);
       }
-      __syncthreads();
-      ix_find_bin(hist, 1 << w, rem, warp_tot, &total, &s_bin, &s_rem);
-      prefix |= (uint32_t)s_bin << sh;
-      mask |= bm << sh;
-      rem = s_rem;
+      atomicAdd(&cnt[pb][b], 1u);
+      atomicMin(&bmin[pb][b], u);
+      atomicMax(&bmax[pb][b], u);
     }
-    if (tid == 0) s_eq = 0;
     __syncthreads();
-    for (int r = 0; r < rounds; ++r) {
-      const int s = r * nthr + tid;
-      const bool valid = s < vis;
-      const uint32_t u = valid ? ix_key(sc[s]) : 0u;
-      const bool eq = valid && u == prefix;
-      const int before = block_exclusive_scan(eq ? 1 : 0, warp_tot, &total);   // equal keys earlier in the round
-      const bool take = valid && (u > prefix || (eq && s_eq + before < rem));
-      const unsigned word = __ballot_sync(0xffffffffu, take);
-      if (lane == 0 && s < vis) bits[s >> 5] = word;
-      __syncthreads();
-      if (tid == 0) s_eq += total;
-      __syncthreads();
+    // this CTA's group sums (64 groups of 32 bins), read by the peers: 4 bins a thread, 8 threads a group
+    {
+      static_assert(kIxBins == 4 * kIxSelThreads, "four bins per thread");
+      const uint4 c4 = reinterpret_cast<const uint4*>(cnt[pb])[tid];
+      uint32_t g = (c4.x + c4.y) + (c4.z + c4.w);
+      g += __shfl_xor_sync(0xffffffffu, g, 1);
+      g += __shfl_xor_sync(0xffffffffu, g, 2);
+      g += __shfl_xor_sync(0xffffffffu, g, 4);
+      if ((tid & 7) == 0) gsum[pb][tid >> 3] = g;
     }
-  }
-  // emit in key order: each thread a contiguous run of words
-  const int wpt = (nwords + nthr - 1) / nthr;
-  const int w0 = tid * wpt, w1 = min(nwords, w0 + wpt);
-  int cnt = 0;
-  for (int i = w0; i < w1; ++i) cnt += __popc(bits[i]);
-  int pos = block_exclusive_scan(cnt, warp_tot, &total);
-  for (int i = w0; i < w1; ++i) {
-    uint32_t m = bits[i];
-    while (m) {
-      const int b = __ffs(m) - 1;
-      m &= m - 1;
-      if (pos < topk) o[pos] = i * 32 + b;   // exactly topk bits are set; the bound keeps a miscount inside
-      ++pos;
+    ix_cluster_sync();                                    // the round's counts are complete in every CTA
+    // the group holding rank `rem` (counted from the top), from the cluster's group sums
+    if (tid < kIxGroups) {
+      const int g = kIxGroups - 1 - tid;                  // thread 0: the top group
+      uint32_t part[kIxSelCtas];
+#pragma unroll
+      for (int r = 0; r < kIxSelCtas; ++r) part[r] = ix_peer(&gsum[pb][0], r)[g];
+      uint32_t t = 0;
+#pragma unroll
+      for (int r = 0; r < kIxSelCtas; ++r) t += part[r];
+      gtot[tid] = t;
     }
+    __syncthreads();
+    if (wid == 0) {
+      // lanes own groups 2 lane and 2 lane + 1 from the top; prefix from the top
+      const int t0 = (int)gtot[2 * lane], t1 = (int)gtot[2 * lane + 1];
+      int inc = t0 + t1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v2 = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += v2;
+      }
+      const int above = inc - t0 - t1;
+      int gsel = -1, grem = 0;
+      if (above < rem && rem <= above + t0) {
+        gsel = kIxGroups - 1 - 2 * lane;
+        grem = rem - above;
+      } else if (above + t0 < rem && rem <= above + t0 + t1) {
+        gsel = kIxGroups - 2 - 2 * lane;
+        grem = rem - above - t0;
+      }
+      const unsigned who = __ballot_sync(0xffffffffu, gsel >= 0);
+      const int src = who ? __ffs(who) - 1 : 0;
+      gsel = __shfl_sync(0xffffffffu, gsel, src);
+      grem = __shfl_sync(0xffffffffu, grem, src);
+      if (gsel < 0) gsel = 0;                             // (not reached: the range holds >= rem keys)
+      // the group's 32 bins over the cluster, lane 0 the top bin
+      const int bin = gsel * 32 + 31 - lane;
+      uint32_t part[kIxSelCtas];
+#pragma unroll
+      for (int r = 0; r < kIxSelCtas; ++r) part[r] = ix_peer(&cnt[pb][0], r)[bin];
+      int cb = 0;
+#pragma unroll
+      for (int r = 0; r < kIxSelCtas; ++r) cb += (int)part[r];
+      int binc = cb;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v2 = __shfl_up_sync(0xffffffffu, binc, o);
+        if (lane >= o) binc += v2;
+      }
+      const int babove = binc - cb;
+      const unsigned hit = __ballot_sync(0xffffffffu, babove < grem && grem <= babove + cb);
+      const int hl = hit ? __ffs(hit) - 1 : 0;
+      const int b = __shfl_sync(0xffffffffu, bin, hl);
+      const int brem = __shfl_sync(0xffffffffu, grem - babove, hl);
+      // the chosen bin's smallest and largest image over the cluster
+      mn = __reduce_min_sync(0xffffffffu, lane < kIxSelCtas ? *ix_peer(&bmin[pb][b], lane) : 0xFFFFFFFFu);
+      mx = __reduce_max_sync(0xffffffffu, lane < kIxSelCtas ? *ix_peer(&bmax[pb][b], lane) : 0u);
+      if (lane == 0) {
+        s_lo = mn;
+        s_hi = mx;
+        s_rem = brem;
+      }
+    }
+    __syncthreads();
+    lo = s_lo;
+    hi = s_hi;
+    rem = s_rem;
   }
+  if (lo < hi && rank == 0 && tid == 0) set_status(p.status, COLI_DEV_SELECT_ROUNDS);
+  const uint32_t thr = lo;     // the topk-th largest image: topk - rem keys lie above it, `rem` equal keys are taken
+
+  // per warp, a contiguous run of the CTA's keys: keys above the threshold and keys equal to it
+  const int seg = ((n + nw - 1) / nw + 31) & ~31;
+  const int w0 = min(n, wid * seg), w1 = min(n, w0 + seg);
+  int n_above = 0, n_eq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? u_s[i] : 0u;
+    n_above += __popc(__ballot_sync(0xffffffffu, i < w1 && u > thr));
+    n_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && u == thr));
+  }
+  const int eq_w = __shfl_sync(0xffffffffu, block_exclusive_scan(lane == 0 ? n_eq : 0, warp_tot, &total), 0);
+  const int eq_cta = total;
+  block_exclusive_scan(lane == 0 ? n_above : 0, warp_tot, &total);
+  const int above_cta = total;
+  if (tid == 0) {
+    ex[2] = (uint32_t)above_cta;
+    ex[3] = (uint32_t)eq_cta;
+  }
+  ix_cluster_sync();                                      // (2) every CTA's counts are visible
+  // keys the lower CTAs place (their keys above, and their share of the equal keys, lowest keys first)
+  int eq_before = 0, placed_before = 0;
+  uint32_t pab[kIxSelCtas], peq[kIxSelCtas];
+#pragma unroll
+  for (int r = 0; r < kIxSelCtas; ++r) {
+    pab[r] = r < (int)rank ? *ix_peer(&ex[2], r) : 0u;
+    peq[r] = r < (int)rank ? *ix_peer(&ex[3], r) : 0u;
+  }
+#pragma unroll
+  for (int r = 0; r < kIxSelCtas; ++r) {
+    placed_before += (int)pab[r] + max(0, min((int)peq[r], rem - eq_before));
+    eq_before += (int)peq[r];
+  }
+  const int eq_base = eq_before + eq_w;                   // equal keys below this warp's run
+  const int take_w = max(0, min(n_eq, rem - eq_base));
+  int pos = placed_before +
+            __shfl_sync(0xffffffffu, block_exclusive_scan(lane == 0 ? n_above + take_w : 0, warp_tot, &total), 0);
+  int eq_seen = eq_base;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? u_s[i] : 0u;
+    const bool eq = i < w1 && u == thr;
+    const unsigned em = __ballot_sync(0xffffffffu, eq);
+    const bool take = i < w1 && (u > thr || (eq && eq_seen + __popc(em & ((1u << lane) - 1u)) < rem));
+    const unsigned tm = __ballot_sync(0xffffffffu, take);
+    if (take) {
+      const int at = pos + __popc(tm & ((1u << lane) - 1u));
+      if (at < topk) o[at] = k0 + i;                    // exactly topk keys are placed; the bound is a guard
+    }
+    pos += __popc(tm);
+    eq_seen += __popc(em);
+  }
+  ix_cluster_sync();                                      // (3) no CTA leaves while a peer may read it
 }
 
 // ------------------------------------------------------------------ host side
 
+static cudaError_t launch_indexer_select(const IndexerCall& c, cudaStream_t st) {
+  IxSel p;
+  p.scores = c.scores;
+  p.ls = c.L;
+  p.L = c.L;
+  p.pos0 = c.pos0;
+  p.topk = c.topk;
+  p.chunk = ((c.L + kIxSelCtas - 1) / kIxSelCtas + 31) & ~31;
+  p.out = c.out;
+  p.status = c.status;
+  const size_t smem = (size_t)(6 * kIxBins + p.chunk) * 4;
+  cudaError_t e = cudaFuncSetAttribute(indexer_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kIxSelCtas, c.T);
+  cfg.blockDim = dim3(kIxSelThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kIxSelCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, indexer_select_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 cudaError_t launch_indexer(const IndexerCall& c, cudaStream_t st, int num_sms) {
   cudaError_t e = c.steps & 1 ? launch_indexer_scores(c, st, num_sms) : cudaSuccess;
-  if (e == cudaSuccess && (c.steps & 2)) {
-    IxSel p;
-    p.scores = c.scores;
-    p.ls = c.L;
-    p.L = c.L;
-    p.pos0 = c.pos0;
-    p.topk = c.topk;
-    p.hist = c.hist;
-    p.chist = c.chist;
-    p.bits = c.sel_bits;
-    p.ws_words = (c.L + 31) / 32;
-    p.cand_val = c.cand_val;
-    p.cand_idx = c.cand_idx;
-    p.cand_n = c.cand_n;
-    p.out = c.out;
-    indexer_mark_kernel<<<dim3((c.L + kIxChunk - 1) / kIxChunk, c.T), kIxMarkThreads, 0, st>>>(p);
-    e = cudaGetLastError();
-    if (e == cudaSuccess) {
-      indexer_finish_kernel<<<c.T, kIxTopkThreads, 0, st>>>(p);
-      e = cudaGetLastError();
-    }
-  }
+  if (e == cudaSuccess && (c.steps & 2)) e = launch_indexer_select(c, st);
   return e;
 }
 
@@ -559,8 +569,6 @@ cudaError_t launch_indexer_scores(const IndexerCall& c, cudaStream_t st, int num
     p.w = c.w + (size_t)t0 * kIxHeads;
     p.scores = c.scores + (size_t)t0 * c.L;
     p.ls = c.L;
-    p.hist = c.hist + ((size_t)t0 << 16);
-    p.chist = c.chist + ((size_t)t0 << 11);
     p.status = c.status;
     p.wait_ns = c.wait_ns;
     indexer_scores_kernel<<<grid, kIxThreads, smem, st>>>(p, kmap, qmap);

@@ -166,13 +166,7 @@ struct IndexerCall {
   const void* q;
   const float* w;
   const void* keys;
-  float* scores;
-  uint32_t* hist;        // [T][65536] score histogram (cleared before the scores are computed)
-  uint32_t* chist;       // [T][2048] coarse score histogram (cleared with it)
-  uint32_t* sel_bits;    // [T][ceil(L / 32)] selected-key bitmask
-  float* cand_val;       // [T][2048] boundary-bin keys
-  int* cand_idx;
-  int* cand_n;           // [T] (cleared before the scores are computed)
+  float* scores;         // [T][L]
   int32_t* out;
   int32_t* status;
   unsigned long long wait_ns;
