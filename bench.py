@@ -181,15 +181,18 @@ def unique_expert_bytes(dl, T, idx=None) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_086_656 + 3_052_288
+DECODE_GATEUP_T1_TRAFFIC = 122_085_888 + 3_308_032
 
 # DRAM bytes per launch of the prefill gate/up grouped GEMM at T=2048, E=256, scaled from the capture
-# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,067,090,944 B read + 17,734,656 B
+# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,081,434,000 B read + 17,477,888 B
 # written).  Both the expert bytes and the gathered activations grow with E and T by the same factor 4
-# (the one shared expert does not: 15 MB of the 4.3 GB); the full-size launch is too large to capture
-# with more than a one-pass metric.  None whenever that kernel changes (it has since that capture: the
-# CTAs no longer run in pairs that share activation tiles).
-PREFILL_GATEUP_T2048_TRAFFIC = None
+# (the one shared expert does not: 15 MB of the 4.4 GB); the full-size launch is too large to capture
+# with more than a one-pass metric.  None whenever that kernel changes.
+PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_081_434_000 + 17_477_888)
+
+# DRAM bytes per launch of the key-selection scores kernel at T=1 over 65,536 keys, from the capture
+# summarised in profiles/indexer_T1_L65536.txt (the key cache read once; the scores stay in L2).
+INDEXER_SCORES_T1_TRAFFIC = 16_813_312
 
 
 def max_over_ranks(v: float, device=None) -> float:
@@ -816,7 +819,10 @@ def bench_indexer(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
         frags[T] = {
             "value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s", "ms_per_step": ms / K,
             "roofline": {"bound": "hbm", "kernel": "indexer_scores", "achieved": ach, "peak": pk["hbm_gbs"],
-                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"], "traffic": None, "peak_source": pk["source"],
+                         "unit": "GB/s", "frac": ach / pk["hbm_gbs"],
+                         "traffic": INDEXER_SCORES_T1_TRAFFIC if (T == 1 and L == 65536) else None,
+                         "duration": "the scores call: the 64-byte status clear and the kernel",
+                         "peak_source": pk["source"],
                          "algorithmic_bytes_per_launch": alg},
             "kernel_ms_per_step": {"indexer_scores": ms_sc / K, "indexer_select": ms_sel / K},
             "e2e": {"value": world * K * T / e2e_s, "unit": "tokens/s",
