@@ -360,10 +360,11 @@ def bench_layer(name: str, args, dev, world: int, want_cpu: bool, cpu_budget_s: 
         }
         del xs
     dl.plan.set_idot(False)
-    cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
     if name == "decode" and not args.experts and not args.tokens and not args.no_cache:
         frags["cache"] = bench_cache(dl, layer, w, args, dev, world)
         frags["pilot"] = bench_pilot(dl, layer, w, args, dev, world)
+    # the oracle last: its threads occupy every host core, and the cache steps are driven from the host
+    cpu = cpu_baseline(w, layer, Ts[0], cpu_budget_s) if want_cpu else None
     dl.close()
     del dl, layer
     torch.cuda.empty_cache()
@@ -844,6 +845,7 @@ def bench_indexer(args, dev, world: int, want_cpu: bool, cpu_budget_s: float):
 def cpu_baseline(w, layer, T: int, budget_s: float):
     """The oracle as it stands on this host's cores (OpenMP over tokens), on a bounded sample of the
     workload's tokens: calls of `cores` tokens each until `budget_s` seconds have passed."""
+    os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")   # idle oracle threads sleep instead of spinning
     import oracle as O
     orc = O.Oracle(layer)
     cores = O.default_threads()

@@ -40,11 +40,12 @@ namespace {
 
 enum KernelId {
   K_ROUTE = 0, K_ROUTER, K_TOPK, K_PERMUTE, K_PREP, K_GATEUP, K_DOWN, K_GATHER, K_TILES, K_TC_GATEUP, K_TC_DOWN,
-  K_COMBINE, K_COUNT
+  K_COMBINE, K_RSPLIT, K_COUNT
 };
 const char* kKernelNames[K_COUNT] = {"route_decode", "router_logits",  "router_topk",    "permute",
                                      "quantize_h",   "expert_gate_up", "expert_down",    "gather_x",
-                                     "plan_tiles",   "tc_gate_up",     "tc_down",        "combine"};
+                                     "plan_tiles",   "tc_gate_up",     "tc_down",        "combine",
+                                     "router_split"};
 
 }  // namespace
 
@@ -167,7 +168,7 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
   w.hq = take(rows * (size_t)p->Fmax * 2);
   w.hqs = take(rows * (size_t)(p->Fmax / kXqBlock) * 8);
   w.y = take(rows * (size_t)d.d * 4);
-  w.xh = w.chunks = w.gu_tiles = w.dn_tiles = w.pf_counts = 0;
+  w.xh = w.chunks = w.gu_tiles = w.dn_tiles = w.pf_counts = w.wsplit = 0;
   if (d.T_max > kDecodeMaxT) {
     const size_t max_chunks = (E + 1) + rows / kPrefillChunk + 2;
     w.xh = take(rows * (size_t)d.d * 2);
@@ -175,6 +176,8 @@ coli_status colibri_moe_plan(const coli_moe_desc* desc, coli_moe_plan_t** plan, 
     w.gu_tiles = take(max_chunks * (size_t)(p->Fmax / kPrefillRows) * 16);
     w.dn_tiles = take(max_chunks * (size_t)(d.d / kPrefillRows) * 16);
     w.pf_counts = take(16);
+    if (d.xtype == COLI_X_BF16 && d.T_max >= kRouterTcMinT && (d.d / kRouterKSplit) % 64 == 0)
+      w.wsplit = take(3 * E * (size_t)d.d * 2);
   }
   w.total = off;
   *workspace_bytes = off;
@@ -340,8 +343,16 @@ coli_status coli::forward_impl(coli_moe_plan* plan, const ExpertTables& tb, Betw
     if ((ce = run(K_ROUTE, [&] { return launch_route_decode(a, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: route_decode");
   } else {
-    if ((ce = run(K_ROUTER, [&] { return launch_router_logits(a, st); })) != cudaSuccess)
+    if (w.wsplit && router_tc_applies(a)) {   // tensor cores, fp32-exact products (router_tc.cu)
+      auto encode = get_encode();
+      if (!encode) return fail(COLI_ECUDA, "forward: cuTensorMapEncodeTiled is not available");
+      if ((ce = run(K_RSPLIT, [&] { return launch_router_split(a, ws + w.wsplit, st); })) != cudaSuccess)
+        return cuda_fail(ce, "forward: router_split");
+      if ((ce = run(K_ROUTER, [&] { return launch_router_tc(a, ws + w.wsplit, encode, st); })) != cudaSuccess)
+        return cuda_fail(ce, "forward: router_logits (tensor cores)");
+    } else if ((ce = run(K_ROUTER, [&] { return launch_router_logits(a, st); })) != cudaSuccess) {
       return cuda_fail(ce, "forward: router_logits");
+    }
     if ((ce = run(K_TOPK, [&] { return launch_router_topk(a, st); })) != cudaSuccess)
       return cuda_fail(ce, "forward: router_topk");
     if ((ce = run(K_PERMUTE, [&] { return launch_permute(a, st); })) != cudaSuccess)

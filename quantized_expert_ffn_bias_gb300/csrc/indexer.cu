@@ -227,9 +227,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
 // kIxSelCtas CTAs (one thread-block cluster) share a query's visible keys in contiguous ranges and keep
 // their keys' integer images in shared memory.  An exact bucket select runs over the cluster: the
 // cluster's smallest and largest image bound the range; each round every CTA counts its keys of the
-// current range in 2048 equal-width bins, the CTAs sum the cluster's counts through distributed shared
-// memory, and the bin holding the topk-th largest key becomes the next range; at most three rounds bring
-// the range to one value (2^32 / 2048^2 < 2048).  Keys above that value are taken, and keys equal to it
+// current range in 2048 bins (round 0 linear in the score value, later rounds in the image), the CTAs
+// sum the cluster's counts through distributed shared memory, and the keys of the bin holding the
+// topk-th largest key become the next range; within four rounds the range is one value.  Keys above
+// that value are taken, and keys equal to it
 // in ascending key order until topk keys are taken (a tie goes to the lower key).  A cluster prefix of
 // the CTAs' counts places each CTA's keys in the ascending output.  Cluster barriers are hardware
 // barriers; no CTA leaves while another may still read its shared memory.

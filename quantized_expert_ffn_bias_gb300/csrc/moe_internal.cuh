@@ -82,6 +82,7 @@ struct WsLayout {
   size_t gu_tiles;     // gate/up tile table (16 B each)
   size_t dn_tiles;     // down tile table (16 B each)
   size_t pf_counts;    // int32[4]: chunks, gate/up tiles, down tiles
+  size_t wsplit;       // bf16 [3][E][d] router weights in three parts (tensor-core router; 0 if unused)
   size_t total;
 };
 
@@ -128,6 +129,13 @@ struct FwdArgs {
 
 cudaError_t launch_route_decode(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_router_logits(const FwdArgs& a, cudaStream_t st);
+// Router logits on the tensor cores (bf16 x, T >= kRouterTcMinT, d / kRouterKSplit a multiple of 64):
+// the fp32 router weights split into three bf16 parts in the workspace, then one grouped MMA pass.
+constexpr int kRouterTcMinT = 128;
+bool router_tc_applies(const FwdArgs& a);
+cudaError_t launch_router_split(const FwdArgs& a, void* wsplit, cudaStream_t st);
+cudaError_t launch_router_tc(const FwdArgs& a, const void* wsplit, PFN_cuTensorMapEncodeTiled_v12000 encode,
+                             cudaStream_t st);
 cudaError_t launch_router_topk(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_permute(const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_quantize_h(const FwdArgs& a, cudaStream_t st);
