@@ -5,7 +5,9 @@
 //
 // Grid: one CTA per expert.  Every CTA builds the full histogram in shared
 // memory (the pair list is small and L2-resident), scans it, and scatters its
-// own expert's pairs with a block-wide ballot prefix.  CTA 0 also writes the
+// own expert's pairs: each warp counts the matches in a contiguous segment of
+// the pairs, and after one block barrier places them with a ballot prefix, so
+// the order stays that of t*k + j.  CTA 0 also writes the
 // offsets, the list of experts that received tokens (ascending ids) and the
 // shared-expert rows.
 #include "moe_internal.cuh"
@@ -18,10 +20,12 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(FwdArgs a) {
   __shared__ int hist[kMaxE];
   __shared__ int scan[kMaxE + 1];
   __shared__ int warp_tot[32];
+  __shared__ int warp_cnt[kPermThreads / 32];
   __shared__ int total;
   const int E = a.E, P = a.T * a.k, tid = threadIdx.x;
   for (int e = tid; e < E; e += kPermThreads) hist[e] = 0;
   __syncthreads();
+#pragma unroll 8
   for (int f = tid; f < P; f += kPermThreads) {
     const int e = a.topk_idx[f];
     if (e < 0 || e >= E) {           // recorded and left out: no row, no output contribution
@@ -48,21 +52,33 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(FwdArgs a) {
   __syncthreads();
 
   const int me = blockIdx.x;
-  if (me < E && hist[me] > 0) {
-    int running = scan[me];
-    const int end = scan[me] + hist[me];
-    for (int f0 = 0; f0 < P && running < end; f0 += kPermThreads) {
-      const int f = f0 + tid;
-      const int m = (f < P && a.topk_idx[f] == me) ? 1 : 0;
-      const int ex = block_exclusive_scan(m, warp_tot, &total);
+  if (me < E && hist[me] > 0) {                 // (block-uniform)
+    constexpr int kWarps = kPermThreads / 32;
+    const int wid = tid >> 5, lane = tid & 31;
+    const int seg = ((P + kWarps - 1) / kWarps + 31) & ~31;
+    const int s0 = min(P, wid * seg), s1 = min(P, s0 + seg);
+    int cnt = 0;
+#pragma unroll 8
+    for (int f0 = s0; f0 < s1; f0 += 32) {
+      const int f = f0 + lane;
+      cnt += __popc(__ballot_sync(0xffffffffu, f < s1 && a.topk_idx[f] == me));
+    }
+    if (lane == 0) warp_cnt[wid] = cnt;
+    __syncthreads();
+    int pos = scan[me];
+    for (int w = 0; w < wid; ++w) pos += warp_cnt[w];
+#pragma unroll 8
+    for (int f0 = s0; f0 < s1; f0 += 32) {
+      const int f = f0 + lane;
+      const bool m = f < s1 && a.topk_idx[f] == me;
+      const unsigned b = __ballot_sync(0xffffffffu, m);
       if (m) {
-        const int pos = running + ex;
-        a.pair_token[pos] = f / a.k;
-        a.pair_slot[pos] = f % a.k;
-        a.pair_of[f] = pos;
+        const int at = pos + __popc(b & ((1u << lane) - 1u));
+        a.pair_token[at] = f / a.k;
+        a.pair_slot[at] = f % a.k;
+        a.pair_of[f] = at;
       }
-      running += total;
-      __syncthreads();
+      pos += __popc(b);
     }
   }
   if (blockIdx.x == 0) {
