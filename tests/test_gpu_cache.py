@@ -115,6 +115,16 @@ def test_cached_forward_equals_resident(torch_cuda, qtype):
         torch.cuda.synchronize()
         assert torch.equal(out, ref), f"packed-tier forward {i} differs from the resident forward"
     assert cache3.stats()["bytes_copied"] == cache3.stats()["misses"] * sb
+    # integer-dot inputs: the cached forward still runs the resident forward's kernels on slots
+    dl.plan.set_idot(True)
+    for i, (c, T) in enumerate([(cache3, 1), (cache3, 2), (cache2, 40)]):
+        xd = to_dev(H.gen_x(51, 400 + i, T, layer.d, H.X_BF16), "cuda")
+        ref = dl.forward(xd).clone()
+        out = torch.full_like(ref, float("nan"))
+        c.forward(T, xd, dl.router_w, dl.bias, out, ws, stream=st)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"integer-dot forward {i} (T={T}) differs from the resident forward"
+    dl.plan.set_idot(False)
     for c in (cache, cache2, small, cache3):
         c.close()
     dl.close()

@@ -58,6 +58,15 @@ def test_noalloc_forward_matches_workspace_forward(torch_cuda):
         if res is not None:
             ref_o = ref_o + res.cpu().numpy().astype(np.float64)[toks]
         check_output(a[toks], ref_o)
+    # integer-dot inputs through the static scratch: the same kernels as the workspace forward
+    dl.plan.set_idot(True)
+    x = to_dev(H.gen_x(31, 7, 3, 1024, H.X_BF16), dl.device)
+    ref = dl.forward(x).clone()
+    out = torch.full((3, 1024), float("nan"), device=dl.device)
+    dl.plan.forward_noalloc(3, x, dl.router_w, dl.bias, out, stream=torch.cuda.current_stream(dl.device))
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref), "integer-dot forward through the static scratch differs"
+    dl.plan.set_idot(False)
     dl.close()
 
 
