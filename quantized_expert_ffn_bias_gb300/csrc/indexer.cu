@@ -53,41 +53,6 @@ __device__ __forceinline__ float ix_unkey(uint32_t k) {
 
 
 
-__device__ __forceinline__ uint64_t ix_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= (uint64_t)1 << 16;                       // leading byte offset (unused for a K-major 128-byte atom)
-  d |= (uint64_t)(1024 >> 4) << 32;             // stride byte offset: next 8 rows
-  d |= (uint64_t)1 << 46;                       // descriptor version
-  d |= (uint64_t)2 << 61;                       // 128-byte swizzle
-  return d;
-}
-
-// kind::f16 instruction descriptor: bf16 A and B, both K-major, fp32 accumulate.
-__device__ __forceinline__ uint32_t ix_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void ix_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void ix_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void ix_tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kIxThreads, 1)
     indexer_scores_kernel(IxArgs p, const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -134,7 +99,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       mbar_arrive_expect_tx(&q_full, (uint32_t)(2 * N * 128));
-      for (int at = 0; at < 2; ++at) ix_tma_load(qs + at * N * 128, &qmap, at * 64, 0, &q_full);
+      for (int at = 0; at < 2; ++at) tma_load_2d_nohint(qs + at * N * 128, &qmap, at * 64, 0, &q_full);
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && !*abort_v; t += gridDim.x, ++it) {
@@ -142,7 +107,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         if (it >= kIxStages && !mbar_wait(&empty[s], ((it / kIxStages) - 1) & 1, p.wait_ns)) { ok = false; break; }
         uint8_t* st = smem + (size_t)s * kIxStageBytes;
         mbar_arrive_expect_tx(&full[s], (uint32_t)kIxStageBytes);
-        for (int at = 0; at < 2; ++at) ix_tma_load(st + at * kIxAtomKeys, &kmap, at * 64, t * kIxKeys, &full[s]);
+        for (int at = 0; at < 2; ++at) tma_load_2d_nohint(st + at * kIxAtomKeys, &kmap, at * 64, t * kIxKeys, &full[s]);
       }
       if (!ok) fail_wait();
       // drain: every issued copy lands before the CTA exits
@@ -153,10 +118,10 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = ix_idesc_bf16(kIxKeys, N);
+      const uint32_t idesc = umma_idesc_bf16(kIxKeys, N);
       bool ok = mbar_wait_spin(&q_full, 0, p.wait_ns);
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint64_t qd = ix_desc_sw128(smem_u32(qs));
+      const uint64_t qd = umma_desc_sw128(smem_u32(qs));
       const uint64_t q_atom = (uint64_t)((N * 128) >> 4);
       int i = 0;
       for (int t = blockIdx.x; ok && t < n_tiles && !*abort_v; t += gridDim.x, ++i) {
@@ -164,17 +129,17 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         if (!mbar_wait_spin(&full[s], (i / kIxStages) & 1, p.wait_ns)) { ok = false; break; }
         if (i >= 2 && !mbar_wait_spin(&acc_empty[acc], ((i >> 1) - 1) & 1, p.wait_ns)) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t kd = ix_desc_sw128(smem_u32(smem + (size_t)s * kIxStageBytes));
+        const uint64_t kd = umma_desc_sw128(smem_u32(smem + (size_t)s * kIxStageBytes));
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           // step kk: 16 elements (32 bytes) of atom kk / 4 of both operands
           const uint64_t off = (uint64_t)((kk & 3) * 2);
           const uint64_t a = kd + off + (kk >= 4 ? (uint64_t)(kIxAtomKeys >> 4) : 0);
           const uint64_t b = qd + off + (kk >= 4 ? q_atom : 0);
-          ix_mma(tmem + (uint32_t)(acc * N), a, b, idesc, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + (uint32_t)(acc * N), a, b, idesc, kk > 0 ? 1u : 0u);
         }
-        ix_commit(&empty[s]);
-        ix_commit(&acc_full[acc]);
+        umma_commit(&empty[s]);
+        umma_commit(&acc_full[acc]);
       }
       if (!ok) fail_wait();
       // the last accumulators must be complete before the CTA frees tensor memory
@@ -192,20 +157,14 @@ __global__ void __launch_bounds__(kIxThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(sp * 32) << 16) + (uint32_t)(acc * N);
       for (int q = 0; q < p.T; ++q) {
         // the query's 64 head columns: four 16-column loads in flight, one wait
-        uint32_t r[kIxHeads];
+        uint32_t r[kIxHeads / 16][16];
 #pragma unroll
-        for (int c = 0; c < kIxHeads / 16; ++c)
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-              : "=r"(r[c * 16 + 0]), "=r"(r[c * 16 + 1]), "=r"(r[c * 16 + 2]), "=r"(r[c * 16 + 3]),
-                "=r"(r[c * 16 + 4]), "=r"(r[c * 16 + 5]), "=r"(r[c * 16 + 6]), "=r"(r[c * 16 + 7]),
-                "=r"(r[c * 16 + 8]), "=r"(r[c * 16 + 9]), "=r"(r[c * 16 + 10]), "=r"(r[c * 16 + 11]),
-                "=r"(r[c * 16 + 12]), "=r"(r[c * 16 + 13]), "=r"(r[c * 16 + 14]), "=r"(r[c * 16 + 15])
-              : "r"(taddr + (uint32_t)(q * kIxHeads + c * 16)));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int c = 0; c < kIxHeads / 16; ++c) tmem_ld16_issue(taddr + (uint32_t)(q * kIxHeads + c * 16), r[c]);
+        tmem_ld_wait();
         float sum = 0.f;
 #pragma unroll
-        for (int j = 0; j < kIxHeads; ++j) sum = fmaf(ws[q * kIxHeads + j], fmaxf(__uint_as_float(r[j]), 0.f), sum);
+        for (int j = 0; j < kIxHeads; ++j)
+          sum = fmaf(ws[q * kIxHeads + j], fmaxf(__uint_as_float(r[j >> 4][j & 15]), 0.f), sum);
         const bool vis = s < p.L && s <= p.pos0 + q;
         if (s < p.L) p.scores[(size_t)q * p.ls + s] = vis ? sum : -INFINITY;
       }

@@ -61,41 +61,6 @@ struct RtArgs {
   unsigned long long wait_ns;
 };
 
-__device__ __forceinline__ uint64_t rt_desc_sw128(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
-  d |= (uint64_t)1 << 16;                       // leading byte offset (unused for a K-major 128-byte atom)
-  d |= (uint64_t)(1024 >> 4) << 32;             // stride byte offset: next 8 rows
-  d |= (uint64_t)1 << 46;                       // descriptor version
-  d |= (uint64_t)2 << 61;                       // 128-byte swizzle
-  return d;
-}
-
-// kind::f16 instruction descriptor: bf16 A and B, both K-major, fp32 accumulate.
-__device__ __forceinline__ uint32_t rt_idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void rt_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-
-__device__ __forceinline__ void rt_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-__device__ __forceinline__ void rt_tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __global__ void __launch_bounds__(kRtThreads, 1)
     router_tc_kernel(RtArgs p, const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -144,8 +109,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
         uint8_t* dst = smem + (size_t)st * kRtStageBytes;
         mbar_arrive_expect_tx(&full[st], (uint32_t)kRtStageBytes);
         const int kx = k0 + s * 64;
-        rt_tma_load(dst, &xmap, kx, t0, &full[st]);
-        for (int q = 0; q < 3; ++q) rt_tma_load(dst + (1 + q) * kRtAtom, &wmap, kx, q * p.E + e0, &full[st]);
+        tma_load_2d_nohint(dst, &xmap, kx, t0, &full[st]);
+        for (int q = 0; q < 3; ++q) tma_load_2d_nohint(dst + (1 + q) * kRtAtom, &wmap, kx, q * p.E + e0, &full[st]);
       }
       if (!ok) fail_wait();
       // drain: every issued copy lands before the CTA exits
@@ -155,28 +120,28 @@ __global__ void __launch_bounds__(kRtThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = rt_idesc_bf16(kRtM, N);
+      const uint32_t idesc = umma_idesc_bf16(kRtM, N);
       bool ok = true;
       int s = 0;
       for (; s < nst && !*abort_v; ++s) {
         const int st = s % kRtStages;
         if (!mbar_wait_spin(&full[st], (s / kRtStages) & 1, p.wait_ns)) { ok = false; break; }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint64_t xd = rt_desc_sw128(smem_u32(smem + (size_t)st * kRtStageBytes));
+        const uint64_t xd = umma_desc_sw128(smem_u32(smem + (size_t)st * kRtStageBytes));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
             // step kk: 16 elements (32 bytes) of the atom, for the weight part q
             const uint64_t off = (uint64_t)(kk * 2);
-            rt_mma(tmem, xd + off, xd + (uint64_t)((1 + q) * kRtAtom >> 4) + off, idesc,
+            umma_ss(tmem, xd + off, xd + (uint64_t)((1 + q) * kRtAtom >> 4) + off, idesc,
                    (s > 0 || kk > 0 || q > 0) ? 1u : 0u);
           }
         }
-        rt_commit(&empty[st]);
+        umma_commit(&empty[st]);
       }
       if (!ok) fail_wait();
-      rt_commit(&acc_full);                   // also after an abort: the epilogue's wait then ends
+      umma_commit(&acc_full);                   // also after an abort: the epilogue's wait then ends
       mbar_wait(&acc_full, 0, p.wait_ns);     // the MMAs are complete before tensor memory is freed
     }
   } else {
@@ -191,12 +156,8 @@ __global__ void __launch_bounds__(kRtThreads, 1)
       const uint32_t taddr = tmem + ((uint32_t)(sp * 32) << 16);
       for (int c = 0; c < N; c += 16) {
         uint32_t r[16];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr + (uint32_t)c));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tmem_ld16_issue(taddr + (uint32_t)c, r);
+        tmem_ld_wait();
         if (t < p.T) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
