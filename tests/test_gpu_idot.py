@@ -60,14 +60,15 @@ def _tau(qtype: int, T: int) -> float:
     return 0.02 if qtype == H.Q_INT8_PC else 0.25
 
 
-def check_hidden(layer, x, hg, idx, pt, ps, tau):
-    """The down kernels' input of every row against the oracle's IDOT hidden step."""
+def check_hidden(layer, x, hg, idx, pt, ps, tau, rows=None):
+    """The down kernels' input of the given rows (default: every row) against the oracle's IDOT hidden
+    step."""
     T, k = idx.shape
     P = T * k
     xf = pins.x_as_f64(x)
     worst = 0.0
     n_near = 0
-    for r in range(hg.shape[0]):
+    for r in (range(hg.shape[0]) if rows is None else rows):
         if r < P:
             t, bank, e, F = int(pt[r]), layer.experts, int(idx[pt[r], ps[r]]), layer.F
         else:
@@ -94,7 +95,9 @@ def check_hidden(layer, x, hg, idx, pt, ps, tau):
     return worst, n_near
 
 
-def run_idot(dl, layer, x, base_rel, base_abs):
+def run_idot(dl, layer, x, base_rel, base_abs, tokens=None):
+    """IDOT forward of x on the device layer, checked against the oracle on `tokens` (default: all): the
+    hidden rows of those tokens' pairs and shared-expert rows, then their outputs."""
     import torch
     from harness.device import to_dev
     T = x.shape[0]
@@ -112,9 +115,15 @@ def run_idot(dl, layer, x, base_rel, base_abs):
     hbuf = torch.empty((rows, Fmax), dtype=torch.float32, device=dl.device)
     dl.plan.debug_hidden(dl.ws, T, hbuf)
     torch.cuda.synchronize()
-    check_hidden(layer, x, hbuf.cpu().numpy(), idx, pt, ps, tau)
+    sel = np.arange(T) if tokens is None else np.asarray(tokens)
+    P = T * layer.k
+    rows = None
+    if tokens is not None:
+        mine = np.isin(pt[:P], sel)
+        rows = list(np.flatnonzero(mine)) + ([P + int(t) for t in sel] if layer.shared is not None else [])
+    check_hidden(layer, x, hbuf.cpu().numpy(), idx, pt, ps, tau, rows)
     # output, on the tokens whose expert set matches the oracle's
-    tok = np.flatnonzero(ov[:, 0] < 0).astype(np.int32)
+    tok = np.intersect1d(np.flatnonzero(ov[:, 0] < 0), sel).astype(np.int32)
     ref, bound = orc.forward_idot(x, tau, tokens=tok)
     err = np.abs(out[tok] - ref)
     excess = np.maximum(err - bound, 0.0)

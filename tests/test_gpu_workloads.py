@@ -78,6 +78,10 @@ def test_decode_T1_T4():
             x = w.x(T, stream)
             rep = run_layer_parity(dl, layer, x)
             print(f"decode T={T}: rel_l2={rep.rel_l2:.2e} max/rms={rep.max_abs_over_rms:.2e} near_ties={rep.near_ties}")
+    # integer-dot inputs at full size, as the bench times them (T=1): every hidden row and the output
+    from tests.test_gpu_idot import run_idot
+    for stream in range(2):
+        run_idot(dl, layer, w.x(1, 10 + stream), 1e-5, 1e-4)
     _release(dl)
 
 
@@ -113,6 +117,11 @@ def test_prefill_T2048_skewed():
     print(f"prefill: loads min={loads.min()} max={loads.max()} idle={int((loads == 0).sum())} "
           f"rel_l2={rep.rel_l2:.2e} near_ties={rep.near_ties}; {len(toks)} outputs checked, covering {desc}")
     assert loads.max() > 400
+    # integer-dot inputs at full size (the bench's IDOT prefill line): the chunk-covering sample of tokens
+    from tests.gpu_parity import MAX_ABS_TOL, REL_L2_TOL
+    from tests.test_gpu_idot import run_idot
+    cover_i, _ = _chunk_cover(dl, 2048, True, 6)
+    run_idot(dl, layer, x, REL_L2_TOL, MAX_ABS_TOL, tokens=np.union1d(_sample(2048, 16, 7), cover_i))
     _release(dl)
 
 
