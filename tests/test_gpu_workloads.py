@@ -82,6 +82,28 @@ def test_decode_T1_T4():
     from tests.test_gpu_idot import run_idot
     for stream in range(2):
         run_idot(dl, layer, w.x(1, 10 + stream), 1e-5, 1e-4)
+    # the expert cache at the bench's configuration (every expert in pinned host memory, 32 device slots):
+    # the cached forward equals the resident forward bit for bit
+    import torch
+    import quantized_expert_ffn_bias_gb300 as coli
+    from harness.device import to_dev
+    from tests.test_gpu_cache import pinned_bank
+    keep, host = pinned_bank(torch, layer.experts)
+    sb = coli.colibri_moe_cache_slot_bytes(dl.plan)
+    S = 4 * layer.k
+    cache = coli.Cache(dl.plan, S, 1.0, host, torch.empty(S * sb, dtype=torch.uint8, device=dl.device), S * sb)
+    ws = torch.empty(dl.plan.workspace_bytes, dtype=torch.uint8, device=dl.device)
+    for step in range(6):
+        xd = to_dev(w.x(1, 20 + step), dl.device)
+        ref = dl.forward(xd).clone()
+        out = torch.full_like(ref, float("nan"))
+        cache.forward(1, xd, dl.router_w, dl.bias, out, ws, stream=torch.cuda.current_stream(dl.device))
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), f"cached decode step {step} differs from the resident forward"
+    s = cache.stats()
+    assert s["lookups"] == 6 * layer.k and s["misses"] > 0
+    cache.close()
+    del keep
     _release(dl)
 
 
