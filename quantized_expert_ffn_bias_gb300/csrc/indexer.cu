@@ -233,6 +233,7 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
   __shared__ uint32_t s_lo, s_hi;
   __shared__ int s_rem;
   __shared__ int warp_tot[32];
+  __shared__ uint32_t wmin[32], wmax[32];
   __shared__ int total;
   const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, wid = tid >> 5, nw = nthr >> 5;
   uint32_t rank;
@@ -250,8 +251,14 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
   const int n = max(0, min(vis, k0 + p.chunk) - k0);
   const float* sc = p.scores + (size_t)q * p.ls + k0;
 
-  // load the images; the CTA's smallest and largest, then the cluster's
+  // load the images; the CTA's smallest and largest, then the cluster's; clear round 0's bins
+  for (int b = tid; b < kIxBins; b += nthr) {
+    cnt[0][b] = 0u;
+    bmin[0][b] = 0xFFFFFFFFu;
+    bmax[0][b] = 0u;
+  }
   uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+#pragma unroll 4
   for (int i = tid; i < n; i += nthr) {
     const uint32_t u = ix_key(__ldcg(sc + i));
     u_s[i] = u;
@@ -261,13 +268,13 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
   mn = __reduce_min_sync(0xffffffffu, mn);
   mx = __reduce_max_sync(0xffffffffu, mx);
   if (lane == 0) {
-    cnt[0][wid] = mn;
-    cnt[1][wid] = mx;
+    wmin[wid] = mn;
+    wmax[wid] = mx;
   }
   __syncthreads();
   if (wid == 0) {
-    mn = __reduce_min_sync(0xffffffffu, lane < nw ? cnt[0][lane] : 0xFFFFFFFFu);
-    mx = __reduce_max_sync(0xffffffffu, lane < nw ? cnt[1][lane] : 0u);
+    mn = __reduce_min_sync(0xffffffffu, lane < nw ? wmin[lane] : 0xFFFFFFFFu);
+    mx = __reduce_max_sync(0xffffffffu, lane < nw ? wmax[lane] : 0u);
     if (lane == 0) {
       ex[0] = mn;
       ex[1] = mx;
@@ -297,13 +304,7 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
     const float vscale = (float)kIxBins / (vhi - vlo);
     const bool by_value = round == 0 && vscale > 0.f && vscale < INFINITY;
     const uint32_t width = (uint32_t)((((uint64_t)hi - lo) >> 11) + 1);
-    for (int b = tid; b < kIxBins; b += nthr) {
-      cnt[pb][b] = 0u;
-      bmin[pb][b] = 0xFFFFFFFFu;
-      bmax[pb][b] = 0u;
-    }
-    __syncthreads();
-    for (int i = tid; i < n; i += nthr) {
+    for (int i = tid; i < n; i += nthr) {                 // (this round's bins were cleared before)
       const uint32_t u = u_s[i];
       if (u < lo || u > hi) continue;
       int b;
@@ -329,6 +330,13 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
       if ((tid & 7) == 0) gsum[pb][tid >> 3] = g;
     }
     ix_cluster_sync();                                    // the round's counts are complete in every CTA
+    // clear the next round's bins: every peer has finished reading them (it passed this barrier after
+    // the round that last used them)
+    for (int b = tid; b < kIxBins; b += nthr) {
+      cnt[pb ^ 1][b] = 0u;
+      bmin[pb ^ 1][b] = 0xFFFFFFFFu;
+      bmax[pb ^ 1][b] = 0u;
+    }
     // the group holding rank `rem` (counted from the top), from the cluster's group sums
     if (tid < kIxGroups) {
       const int g = kIxGroups - 1 - tid;                  // thread 0: the top group
@@ -410,28 +418,37 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
     n_above += __popc(__ballot_sync(0xffffffffu, i < w1 && u > thr));
     n_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && u == thr));
   }
-  const int eq_w = __shfl_sync(0xffffffffu, block_exclusive_scan(lane == 0 ? n_eq : 0, warp_tot, &total), 0);
-  const int eq_cta = total;
-  block_exclusive_scan(lane == 0 ? n_above : 0, warp_tot, &total);
-  const int above_cta = total;
+  // one scan of both counts, packed (each below 2^16: a CTA holds at most 16384 keys)
+  const int packed_w = __shfl_sync(0xffffffffu, block_exclusive_scan(lane == 0 ? (n_eq << 16) | n_above : 0, warp_tot,
+                                                                     &total), 0);
+  const int eq_w = packed_w >> 16;
+  const int eq_cta = total >> 16, above_cta = total & 0xFFFF;
   if (tid == 0) {
     ex[2] = (uint32_t)above_cta;
     ex[3] = (uint32_t)eq_cta;
   }
   ix_cluster_sync();                                      // (2) every CTA's counts are visible
-  // keys the lower CTAs place (their keys above, and their share of the equal keys, lowest keys first)
-  int eq_before = 0, placed_before = 0;
-  uint32_t pab[kIxSelCtas], peq[kIxSelCtas];
+  // keys the lower CTAs place (their keys above, and their share of the equal keys, lowest keys first):
+  // lane r of warp 0 reads CTA r's counts, a warp scan orders them
+  if (wid == 0) {
+    const bool lower = lane < (int)rank;
+    const int ab = lower ? (int)*ix_peer(&ex[2], lane) : 0, eq = lower ? (int)*ix_peer(&ex[3], lane) : 0;
+    int inc = eq;
 #pragma unroll
-  for (int r = 0; r < kIxSelCtas; ++r) {
-    pab[r] = r < (int)rank ? *ix_peer(&ex[2], r) : 0u;
-    peq[r] = r < (int)rank ? *ix_peer(&ex[3], r) : 0u;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t2 = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += t2;
+    }
+    const int placed = ab + max(0, min(eq, rem - (inc - eq)));
+    const int placed_sum = __reduce_add_sync(0xffffffffu, placed);
+    const int eq_sum = __shfl_sync(0xffffffffu, inc, 31);
+    if (lane == 0) {
+      wmin[0] = (uint32_t)placed_sum;
+      wmax[0] = (uint32_t)eq_sum;
+    }
   }
-#pragma unroll
-  for (int r = 0; r < kIxSelCtas; ++r) {
-    placed_before += (int)pab[r] + max(0, min((int)peq[r], rem - eq_before));
-    eq_before += (int)peq[r];
-  }
+  __syncthreads();
+  const int placed_before = (int)wmin[0], eq_before = (int)wmax[0];
   const int eq_base = eq_before + eq_w;                   // equal keys below this warp's run
   const int take_w = max(0, min(n_eq, rem - eq_base));
   int pos = placed_before +
@@ -451,7 +468,9 @@ __global__ void __launch_bounds__(kIxSelThreads, 1) indexer_select_kernel(IxSel 
     pos += __popc(tm);
     eq_seen += __popc(em);
   }
-  ix_cluster_sync();                                      // (3) no CTA leaves while a peer may read it
+  // (3) no CTA leaves while a peer may read it.  Relaxed: no data crosses this barrier, and every peer load
+  // of this CTA's shared memory was consumed before its arrival; the index stores need no cluster release.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ host side
