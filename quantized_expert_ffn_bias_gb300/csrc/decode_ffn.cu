@@ -66,18 +66,20 @@ __device__ __forceinline__ int block_rows() { return DOWN ? kRows : kRows / 2; }
 
 template <bool DOWN>
 __device__ __forceinline__ bool get_unit(const FwdArgs& a, int u, int n_routed, Unit& out) {
+  // the shared expert's units first (it carries every token), then the routed experts' in unit-table
+  // order (most tokens first)
   const int rows = block_rows<DOWN>();
   const int per_routed = (DOWN ? a.d : a.F) / rows;
-  const int routed_units = n_routed * per_routed;
+  const int per_shared = a.has_shared ? (DOWN ? a.d : a.Fs) / rows : 0;
   int i, rb;
-  if (u < routed_units) {
+  if (u < per_shared) {
+    i = n_routed;
+    rb = u;
+  } else {
+    u -= per_shared;
+    if (u >= n_routed * per_routed) return false;
     i = u / per_routed;
     rb = u % per_routed;
-  } else {
-    const int per_shared = (DOWN ? a.d : a.Fs) / rows;
-    if (!a.has_shared || u - routed_units >= per_shared) return false;
-    i = n_routed;
-    rb = u - routed_units;
   }
   const int4 e = __ldcg(a.utab + i);      // (expert, first pair row, pairs), written by the routing kernel
   out.slot = a.slot_of ? __ldg(a.slot_of + e.x) : e.x;   // where the expert's weights are stored

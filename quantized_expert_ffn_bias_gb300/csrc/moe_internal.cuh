@@ -64,7 +64,7 @@ struct WsLayout {
   size_t pair_slot;    // int32 [P_max]
   size_t pair_of;      // int32 [P_max]
   size_t unique;       // int32 [E+1]
-  size_t utab;         // int4 [E+1]: per entry of unique (+ shared): (slot, first pair row, pairs, 0); decode only
+  size_t utab;         // int4 [E+1]: (slot, first pair row, pairs, 0) per expert with tokens, most pairs first, then the shared expert; decode only
   size_t n_unique;     // int32 [4]
   size_t logits;       // float [kRouterKSplit][T_max][E]
   size_t xs;           // float [T_max][d]  (dequant-GEMV input, pre-scaled)

@@ -343,6 +343,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
   extern __shared__ float sm[];
   __shared__ int is_last;
   __shared__ int hist[kDecodeMaxT * kMaxK];   // grouping: first pair of its expert
+  __shared__ int ucnt[kDecodeMaxT * kMaxK];   // grouping: pairs of the expert of a first pair
   __shared__ int sidx[kDecodeMaxT * kMaxK];
   const int tid = threadIdx.x, lane = tid & 31;
   griddep_launch_dependents();     // the expert kernel may start its prologue
@@ -512,19 +513,30 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(FwdArgs a) 
     for (int t = tid; t < a.T; t += kRouteThreads) a.pair_token[P + t] = t;
   __syncthreads();
   // experts with tokens, ascending: rank of each expert's first pair among the
-  // first pairs; utab gets (slot, first pair row, pairs) per entry for the
-  // dequant-GEMV kernels
+  // first pairs.  utab gets (slot, first pair row, pairs) per entry for the
+  // dequant-GEMV kernels, ordered by pairs, most first (ties: ascending id):
+  // units are dealt in utab order, so the experts that take several passes
+  // start in the first round instead of lengthening the last one
+  for (int f = tid; f < P; f += kRouteThreads) {
+    int cnt = 0;
+    if (hist[f]) {
+      const int e = sidx[f];
+      for (int g = 0; g < P; ++g) cnt += sidx[g] == e;
+    }
+    ucnt[f] = cnt;                   // pairs of the expert whose first pair f is (0: not a first pair)
+  }
+  __syncthreads();
   for (int f = tid; f < P; f += kRouteThreads) {
     if (!hist[f]) continue;
-    const int e = sidx[f];
-    int r = 0, below = 0, cnt = 0;
+    const int e = sidx[f], cnt = ucnt[f];
+    int r = 0, below = 0, ro = 0;
     for (int g = 0; g < P; ++g) {
       r += hist[g] && sidx[g] < e;
       below += sidx[g] < e;
-      cnt += sidx[g] == e;
+      ro += hist[g] && (ucnt[g] > cnt || (ucnt[g] == cnt && sidx[g] < e));
     }
     a.unique[r] = e;
-    a.utab[r] = make_int4(e, below, cnt, 0);
+    a.utab[ro] = make_int4(e, below, cnt, 0);
   }
   if (tid == 0) {
     int nu = 0;
