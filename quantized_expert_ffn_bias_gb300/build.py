@@ -2,6 +2,7 @@
 compiled in parallel, linked into ``_build/libcolibri_moe.so`` beside this file."""
 from __future__ import annotations
 
+import fcntl
 import glob
 import os
 import shutil
@@ -45,6 +46,18 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    # one builder at a time (parallel test workers may all find the library stale)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():
+                return LIB
+            return _build(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build(verbose: bool) -> str:
     nv = nvcc()
     procs, objs = [], []
     for src in sources():
