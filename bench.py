@@ -181,14 +181,14 @@ def unique_expert_bytes(dl, T, idx=None) -> tuple[int, int]:
 # profiles/decode_ffn_int4_T1_E32.txt (dram__bytes_read.sum + dram__bytes_write.sum of the T=1 gate/up
 # launch; the launch reads the 8 selected experts, the same bytes as with E=256).  Set to None whenever
 # that kernel changes, until it is captured again.
-DECODE_GATEUP_T1_TRAFFIC = 122_085_888 + 3_308_032
+DECODE_GATEUP_T1_TRAFFIC = 122_084_096 + 3_338_240
 
 # DRAM bytes per launch of the prefill gate/up grouped GEMM at T=2048, E=256, scaled from the capture
-# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,081,434,000 B read + 17,477,888 B
+# summarised in profiles/prefill_ffn_int4_E64_T512.txt (T=512, E=64: 1,081,396,000 B read + 17,395,456 B
 # written).  Both the expert bytes and the gathered activations grow with E and T by the same factor 4
 # (the one shared expert does not: 15 MB of the 4.4 GB); the full-size launch is too large to capture
 # with more than a one-pass metric.  None whenever that kernel changes.
-PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_081_434_000 + 17_477_888)
+PREFILL_GATEUP_T2048_TRAFFIC = 4 * (1_081_396_000 + 17_395_456)
 
 # DRAM bytes per launch of the key-selection scores kernel at T=1 over 65,536 keys, from the capture
 # summarised in profiles/indexer_T1_L65536.txt (the key cache read once; the scores stay in L2).
