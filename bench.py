@@ -25,6 +25,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import contextlib
 import json
 import os
 import statistics
@@ -378,7 +379,8 @@ def _host_tier(dl, layer):
     import quantized_expert_ffn_bias_gb300 as coli
     sb = coli.colibri_moe_cache_slot_bytes(dl.plan)
     offs = coli.cache_slot_offsets(layer.d, layer.F, layer.qtype)
-    keep = torch.empty((layer.E, sb), dtype=torch.uint8).pin_memory()
+    with near_gpu(dl.device):          # the pages lie in the memory of the GPU's own host
+        keep = torch.empty((layer.E, sb), dtype=torch.uint8, pin_memory=True)
     kn = keep.numpy()
     for e in range(layer.E):
         for j, (n, part) in enumerate((n, p) for n in ("gate", "up", "down") for p in ("q", "s", "z")):
@@ -393,11 +395,51 @@ def _host_tier(dl, layer):
     return keep, host, sb
 
 
+def _gpu_numa(dev):
+    """(NUMA node, its host cores) of the GPU's PCI device from sysfs, or None."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        base = f"/sys/bus/pci/devices/{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        with open(base + "/numa_node") as f:
+            node = int(f.read().strip())
+        if node < 0:
+            return None
+        with open(f"/sys/devices/system/node/node{node}/cpulist") as f:
+            cpus = set()
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        return node, cpus
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
+@contextlib.contextmanager
+def near_gpu(dev):
+    """Run the block on the host cores of the GPU's NUMA node, so that pinned host memory allocated in it
+    lies in that node's memory (first touch) and host-to-device copies take the GPU's own host link.
+    Yields the node, or None where sysfs does not name one (then nothing changes)."""
+    loc = _gpu_numa(dev)
+    if loc is None:
+        yield None
+        return
+    node, cpus = loc
+    old = os.sched_getaffinity(0)
+    try:
+        os.sched_setaffinity(0, (cpus & old) or cpus)
+        yield node
+    finally:
+        os.sched_setaffinity(0, old)
+
+
 def host_link_gbs(sb: int, dev, n: int = 8) -> float:
     """The host-to-device rate of this GPU's host link: n expert slots (sb bytes each) copied from pinned host
     memory in one copy, best of 3 (CUDA events).  The denominator of the expert-cache rooflines."""
     import torch
-    src = torch.empty(n * sb, dtype=torch.uint8).pin_memory()
+    with near_gpu(dev):
+        src = torch.empty(n * sb, dtype=torch.uint8, pin_memory=True)
+        src.fill_(1)
     dst = torch.empty(n * sb, dtype=torch.uint8, device=dev)
     st = torch.cuda.current_stream(dev)
     best = 0.0
@@ -479,7 +521,7 @@ def bench_cache(dl, layer, w, args, dev, world: int):
         "cache": {"slots": S, "weight": weight, "hit_rate": hit, "lookups": st_["lookups"], "misses": st_["misses"],
                   "bytes_copied_per_step": st_["bytes_copied"] / K,
                   "simulated_hit_rate_plain_lru": timed_hits(0.0), "simulated_hit_rate_weighted": timed_hits(weight),
-                  "host_pin_s": round(pin_s, 1)},
+                  "host_pin_s": round(pin_s, 1), "host_numa_node": (_gpu_numa(dev) or (None,))[0]},
         "e2e": {"value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": st_["bytes_copied"] / K, "d2h_bytes_per_step": 0},
         "gpu_launches": K * dl.plan.last_launch_count(),
