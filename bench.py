@@ -454,6 +454,23 @@ def host_link_gbs(sb: int, dev, n: int = 8) -> float:
     return best
 
 
+def tier_copy_gbs(keep, sb: int, dev, n: int = 8) -> float:
+    """The host-to-device rate out of the cache's own host tier: n experts copied in one copy, best of 3."""
+    import torch
+    src = keep.view(-1)[: n * sb]
+    dst = torch.empty(n * sb, dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream(dev)
+    best = 0.0
+    for _ in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        dst.copy_(src, non_blocking=True)
+        e1.record(st)
+        torch.cuda.synchronize(dev)
+        best = max(best, n * sb / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    return best
+
+
 def bench_cache(dl, layer, w, args, dev, world: int):
     """Decode at T=1 with the experts in host memory behind a 32-slot device cache (4 x k slots, the
     walkthrough page's default), router bias Zipf-skewed (as in the prefill workload) so that experts recur.
@@ -507,6 +524,7 @@ def bench_cache(dl, layer, w, args, dev, world: int):
     hit = st_["hits"] / max(1, st_["lookups"])
     copy_s = ms * 1e-3
     link = host_link_gbs(sb, dev)
+    tier = tier_copy_gbs(keep, sb, dev)
     ach = st_["bytes_copied"] / copy_s / 1e9
     cache.close()
     del keep, slots
@@ -521,7 +539,8 @@ def bench_cache(dl, layer, w, args, dev, world: int):
         "cache": {"slots": S, "weight": weight, "hit_rate": hit, "lookups": st_["lookups"], "misses": st_["misses"],
                   "bytes_copied_per_step": st_["bytes_copied"] / K,
                   "simulated_hit_rate_plain_lru": timed_hits(0.0), "simulated_hit_rate_weighted": timed_hits(weight),
-                  "host_pin_s": round(pin_s, 1), "host_numa_node": (_gpu_numa(dev) or (None,))[0]},
+                  "host_pin_s": round(pin_s, 1), "host_numa_node": (_gpu_numa(dev) or (None,))[0],
+                  "tier_copy_gbs": tier},
         "e2e": {"value": replica_tokens_per_s(world, K, T, ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": st_["bytes_copied"] / K, "d2h_bytes_per_step": 0},
         "gpu_launches": K * dl.plan.last_launch_count(),
