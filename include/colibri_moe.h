@@ -335,7 +335,9 @@ COLI_API coli_status colibri_moe_profile_end(coli_moe_plan_t* plan, coli_kernel_
  *   experts than there are slots.
  * colibri_moe_cache_prefetch: load the given experts (host array of ids) ahead
  *   of use on `stream` (e.g. the next layer's predicted experts).  It must not
- *   run while a forward of the same cache reads the slots on another stream.
+ *   run while a forward of the same cache reads the slots on another stream:
+ *   order `stream` after such forwards (an event), and the next forward after
+ *   the prefetch copies.
  * colibri_moe_cache_stats / _reset_stats: counters since creation or reset
  *   (cache_hit_rate = hits / lookups).
  * colibri_moe_cache_resident: HOST array [E] receives each expert's slot or -1.
@@ -377,8 +379,11 @@ COLI_API void colibri_moe_cache_destroy(coli_cache_t* cache);
  * [min(E, T*k)], may be NULL) and *n_predicted receive the predicted experts
  * in ascending order.  workspace: a workspace of plan_next that no running
  * forward uses.  Use a stream other than the current layer's so that the
- * copies overlap its compute.  Errors as colibri_moe_forward and
- * colibri_moe_cache_prefetch.
+ * copies overlap its compute; as with colibri_moe_cache_prefetch, `stream`
+ * must be ordered after every earlier forward of cache_next that may still
+ * read its slots (e.g. wait on an event recorded after that forward), and the
+ * next forward of cache_next must wait for the prefetch copies.  Errors as
+ * colibri_moe_forward and colibri_moe_cache_prefetch.
  */
 COLI_API coli_status colibri_moe_cache_pilot(coli_moe_plan_t* plan_next, coli_cache_t* cache_next, int T, const void* x,
                                              const float* router_w, const float* bias, int32_t* predicted,
