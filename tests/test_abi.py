@@ -59,6 +59,22 @@ def test_plan_valid_and_workspace_grows_with_T(L):
     L.colibri_moe_destroy(h)
 
 
+def test_plan_reserves_split_router_weights_for_tensor_core_routing(L):
+    """Plans that may run the tensor-core router (bf16 x, T_max >= 128) hold the router weights in three bf16
+    parts, [3][E][d]; fp32-x plans and smaller T_max do not."""
+    sizes = {}
+    for xt in (coli.COLI_X_BF16, coli.COLI_X_F32):
+        for T in (127, 128):
+            rc, h, n = _plan(L, _desc(T_max=T, xtype=xt))
+            assert rc == coli.COLI_OK
+            L.colibri_moe_destroy(h)
+            sizes[xt, T] = n
+    grow_bf16 = sizes[coli.COLI_X_BF16, 128] - sizes[coli.COLI_X_BF16, 127]
+    grow_f32 = sizes[coli.COLI_X_F32, 128] - sizes[coli.COLI_X_F32, 127]
+    assert grow_bf16 - grow_f32 == 3 * 16 * 512 * 2
+    assert sizes[coli.COLI_X_BF16, 127] == sizes[coli.COLI_X_F32, 127]
+
+
 @pytest.mark.parametrize("bad,status", [
     (dict(k=0), coli.COLI_EINVAL),
     (dict(k=17), coli.COLI_EINVAL),            # k > E
